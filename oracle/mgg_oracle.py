@@ -1,0 +1,370 @@
+"""Plain, slow, float64 CPU oracle of the MoE variable-size grouped GEMM.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): only tests, smoke() and
+bench.py's CPU-baseline leg may use it.  It is independent of the CUDA path.
+
+Notation (shared by the three pages): E experts share K (contraction) and N
+(output width); expert e receives m_e rows, sum_e m_e = T*k
+[P3 "Grouped GEMM" §1].  Weights are stored [E, N, K] like nn.Linear, so the
+expert product is Y_e = X_e W_e^T [P1 "Grouped GEMM for MoE, in depth",
+§Data layout, offsets and alignment; P2 "grouped-gemm-moe", §Usage].
+Assignment a = t*k + j is token t's j-th routed copy, with expert ids[t, j]
+and routing weight w[t, j].
+
+Inputs are numpy arrays.  Values the GPU consumes as bfloat16 are passed in
+already bfloat16-valued (widened exactly to float64 by the caller); the only
+roundings the oracle performs itself are the ones the method performs on
+intermediate operands (``bf16_round``, ``fp32_mul``).  Every accumulation is
+float64.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+__all__ = [
+    "bf16_round", "fp32_mul", "Routing", "route", "end_offsets", "tile_schedule",
+    "schedule_stats", "grouped_gemm", "moe_forward", "moe_forward_unfused",
+    "moe_backward", "moe_backward_rows", "moe_backward_dw_rows", "masked_grouped_gemm",
+    "moe_loss", "rel_frobenius", "max_abs_ratio",
+]
+
+
+# --------------------------------------------------------------------------
+# Roundings the method applies to intermediate operands
+# --------------------------------------------------------------------------
+def bf16_round(a) -> np.ndarray:
+    """float32 -> bfloat16 round-to-nearest-even, returned as float64 values.
+
+    Written from the IEEE-754 definition: bfloat16 keeps the top 16 bits of the
+    binary32 pattern; the dropped 16 bits round to nearest, ties to the even
+    kept pattern.  Overflow rounds to infinity; NaN stays NaN.  Used for the
+    backward operands the pages leave at "bf16 activations" [P2 §Requirements
+    and limits]: dy and w*dy are consumed by the tensor cores as bfloat16.
+    """
+    a32 = np.ascontiguousarray(a, dtype=np.float32)
+    bits = a32.view(np.uint32).astype(np.uint64)
+    keep = bits >> 16
+    low = bits & 0xFFFF
+    round_up = (low > 0x8000) | ((low == 0x8000) & ((keep & 1) == 1))
+    keep = keep + round_up.astype(np.uint64)
+    out = (keep << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    out[np.isnan(a32)] = np.nan
+    return out.reshape(a32.shape)
+
+
+def fp32_mul(a, b) -> np.ndarray:
+    """Correctly rounded float32 product fl32(a*b), returned as float64."""
+    return (np.asarray(a, dtype=np.float32) * np.asarray(b, dtype=np.float32)).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# Routing: histogram, offsets, stable permutation  [P1 §Data layout; P2 §How it works;
+# P3 §4.1 Permute]
+# --------------------------------------------------------------------------
+@dataclass
+class Routing:
+    counts: np.ndarray      # [E]   m_e
+    end_offs: np.ndarray    # [E]   inclusive prefix sums (end offset of each group)
+    start: np.ndarray       # [E+1] exclusive prefix sums, start[E] = S
+    row_assign: np.ndarray  # [S]   sorted row r -> assignment a
+    row_token: np.ndarray   # [S]   sorted row r -> token t = a // k
+    row_weight: np.ndarray  # [S]   sorted row r -> routing weight w_a
+
+
+def end_offsets(group_sizes) -> np.ndarray:
+    """int32 end offsets: offs[e] = sum_{e' <= e} m_e'.
+
+    Counts [3, 0, 5] give [3, 3, 8]; group e is rows offs[e-1] .. offs[e]-1
+    [P1 §Data layout, offsets and alignment].
+    """
+    sizes = np.asarray(group_sizes, dtype=np.int64)
+    return np.cumsum(sizes).astype(np.int32)
+
+
+def route(expert_ids, topk_weights, E: int) -> Routing:
+    """Sort the S = T*k assignments by expert, stably.
+
+    The pages turn routing into a sort by expert giving a row->token map, a
+    per-row routing weight and per-expert group sizes [P2 §How it works]; the
+    sort is stable on the flattened ids [P1 §Data layout, argsort(stable)],
+    so ties keep ascending assignment order a = t*k + j.  The same index is
+    used to permute and (reversed) to un-permute [P3 §4.3].
+    """
+    ids = np.asarray(expert_ids).reshape(-1).astype(np.int64)
+    k = np.asarray(expert_ids).shape[1]
+    w = np.asarray(topk_weights, dtype=np.float32).reshape(-1)
+    counts = np.bincount(ids, minlength=E).astype(np.int32)
+    end_offs = end_offsets(counts)
+    start = np.concatenate([[0], end_offs]).astype(np.int32)
+    row_assign = np.argsort(ids, kind="stable").astype(np.int32)
+    row_token = (row_assign // k).astype(np.int32)
+    row_weight = w[row_assign]
+    return Routing(counts, end_offs, start, row_assign, row_token, row_weight)
+
+
+# --------------------------------------------------------------------------
+# Tile schedule  [P1 §Problem descriptors and the tile scheduler; P3 §4.2]
+# --------------------------------------------------------------------------
+def tile_schedule(counts, N: int, BM: int, BN: int) -> dict:
+    """Flat tile space over all experts.
+
+    Expert e contributes ceil(m_e/BM) * ceil(N/BN) tiles; an exclusive prefix
+    sum gives each expert's first tile and the total is the length of the flat
+    space [P1 §Problem descriptors].  Inside an expert tiles are walked
+    column-block-major (all row blocks of column block 0, then column block
+    1, ...) so consecutive tiles reuse the same weight tile [P1, same section,
+    "Two details matter for speed"].  A tile never spans two experts; the last
+    row block of an expert is ragged: rows = min(BM, m_e - mb*BM).
+
+    Returns tile_start [E+1] and tiles [total, 5] with columns
+    (e, mb, nb, row0, rows), row0 being the first sorted row of the tile.
+    Written as an enumeration in expert order, not as a search.
+    """
+    counts = np.asarray(counts, dtype=np.int64)
+    E = counts.size
+    tiles_n = -(-N // BN)
+    tiles_m = -(-counts // BM)
+    per_expert = tiles_m * tiles_n
+    tile_start = np.concatenate([[0], np.cumsum(per_expert)]).astype(np.int64)
+    start = np.concatenate([[0], np.cumsum(counts)])
+    rows_out = []
+    for e in range(E):
+        for nb in range(tiles_n):
+            for mb in range(int(tiles_m[e])):
+                row0 = int(start[e]) + mb * BM
+                rows = min(BM, int(counts[e]) - mb * BM)
+                rows_out.append((e, mb, nb, row0, rows))
+    tiles = np.array(rows_out, dtype=np.int64).reshape(-1, 5)
+    return {"tile_start": tile_start, "tiles": tiles, "tiles_n": tiles_n}
+
+
+def schedule_stats(counts, N: int, BM: int, BN: int, num_sms: int) -> dict:
+    """Row blocks, tiles, waves and useful-row fraction of a schedule.
+
+    Waves = ceil(tiles / num_sms) for a persistent kernel with one CTA per SM;
+    useful-row fraction = real rows / computed rows, computed rows being
+    row blocks * BM [P1 §Worked example: tile counts under skew; §What to do
+    next, item 3].
+    """
+    counts = np.asarray(counts, dtype=np.int64)
+    row_blocks = int((-(-counts // BM)).sum())
+    tiles_n = -(-N // BN)
+    tiles = row_blocks * tiles_n
+    computed = row_blocks * BM
+    real = int(counts.sum())
+    return {
+        "row_blocks": row_blocks,
+        "tiles": tiles,
+        "waves": -(-tiles // num_sms),
+        "waves_exact": tiles / num_sms,
+        "computed_rows": computed,
+        "real_rows": real,
+        "useful_fraction": real / computed if computed else 1.0,
+    }
+
+
+# --------------------------------------------------------------------------
+# Bare grouped GEMM  [P2 §How it works, "with the permutation maps omitted";
+# P1 §Persistent grouped GEMM pseudocode]
+# --------------------------------------------------------------------------
+def grouped_gemm(A, W, end_offs) -> np.ndarray:
+    """C[r, :] = A[r, :] W_g^T for the group g whose rows contain r.
+
+    Rows are pre-grouped; group g is rows end_offs[g-1] .. end_offs[g]-1
+    (end_offs[-1] taken as 0).  A per-group loop, as in the loop reference of
+    P1 §Data layout ("reference()").
+    """
+    A = np.asarray(A, dtype=np.float64)
+    C = np.zeros((A.shape[0], W.shape[1]))
+    lo = 0
+    for g, hi in enumerate(np.asarray(end_offs, dtype=np.int64)):
+        if hi > lo:
+            C[lo:hi] = A[lo:hi] @ np.asarray(W[g], dtype=np.float64).T
+        lo = hi
+    return C
+
+
+# --------------------------------------------------------------------------
+# Fused MoE forward  [P2 §How it works; §Correctness "pure-torch MoE"]
+# --------------------------------------------------------------------------
+def moe_forward(x, W, expert_ids, topk_weights, tokens=None) -> np.ndarray:
+    """Route (i), per assignment: y[t] = sum_j w[t,j] * x[t] W_{ids[t,j]}^T.
+
+    The top-k combine by routing weight of the pages' MoE layer [P2 intro;
+    P3 §4.3], evaluated directly per (slot j, expert e) with no permutation.
+    ``tokens`` restricts the output to those token rows (for sampled checks
+    at full size).
+    """
+    ids = np.asarray(expert_ids)
+    w = np.asarray(topk_weights, dtype=np.float64)
+    x = np.asarray(x, dtype=np.float64)
+    tok = np.arange(ids.shape[0]) if tokens is None else np.asarray(tokens)
+    y = np.zeros((tok.size, W.shape[1]))
+    for j in range(ids.shape[1]):
+        for e in range(W.shape[0]):
+            sel = np.nonzero(ids[tok, j] == e)[0]
+            if sel.size:
+                t = tok[sel]
+                y[sel] += w[t, j][:, None] * (x[t] @ np.asarray(W[e], dtype=np.float64).T)
+    return y
+
+
+def moe_forward_unfused(x, W, expert_ids, topk_weights) -> np.ndarray:
+    """Route (ii): explicit gather -> per-expert GEMM loop -> scatter-combine.
+
+    The unfused path the pages compare the fused kernel with [P2 §Correctness,
+    "The fusion is exact"; P3 §4 data flow permute -> GEMM -> un-permute]:
+    X_s = x[row_token], Y_s[group e] = X_s[group e] W_e^T, then
+    y[row_token[r]] += row_weight[r] * Y_s[r] in sorted-row order.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    T = x.shape[0]
+    E, N = W.shape[0], W.shape[1]
+    r = route(expert_ids, topk_weights, E)
+    Xs = x[r.row_token]
+    Ys = np.empty((Xs.shape[0], N))
+    for e in range(E):
+        lo, hi = r.start[e], r.start[e + 1]
+        if hi > lo:
+            Ys[lo:hi] = Xs[lo:hi] @ np.asarray(W[e], dtype=np.float64).T
+    y = np.zeros((T, N))
+    for row in range(Xs.shape[0]):
+        y[r.row_token[row]] += np.float64(r.row_weight[row]) * Ys[row]
+    return y
+
+
+def moe_loss(dy, y) -> float:
+    """L = sum(dy * y), the scalar whose gradients the backward returns."""
+    return float(np.sum(np.asarray(dy, dtype=np.float64) * y))
+
+
+# --------------------------------------------------------------------------
+# Backward  [P1 §The backward pass; P2 §How it works, backward paragraph]
+# --------------------------------------------------------------------------
+def _dyw_operand(w_col, dy_rows, bf16_operands):
+    # the dW operand a_a = w_a * dy[t(a)]: rounded to fp32 then bfloat16 on the
+    # bfloat16 path, exact otherwise
+    if bf16_operands:
+        return bf16_round(fp32_mul(w_col[:, None], dy_rows))
+    return w_col[:, None].astype(np.float64) * dy_rows
+
+
+def moe_backward(dy, x, W, expert_ids, topk_weights, bf16_operands: bool = True):
+    """Gradients of L = sum(dy * y) with y = moe_forward(x, W, ids, w).
+
+    * dX_g = dY_g W_g (the forward pattern with W read transposed), combined
+      back per token with the routing weight: dx[t] = sum_j w[t,j] dy[t] W_e
+      [P1 §The backward pass, input gradient].
+    * dW_e = sum over e's assignments of (w_a dy[t(a)])^T x[t(a)], a
+      reduction over the jagged dimension; an expert with no rows gets
+      exactly zero [P1 §The backward pass, weight gradient and its trap].
+    * dtopk[t,j] = <dy[t], x[t] W_e^T>: the incoming gradient against the
+      unweighted per-assignment product [P2 §How it works].
+
+    With ``bf16_operands`` the tensor-core operands are rounded as the GPU
+    consumes them: dy -> bf16(dy) for dX and dtopk, and w*dy ->
+    bf16(fl32(w*dy)) for dW.  Returns (dx [T,K], dW [E,N,K], dtopk [T,k]).
+    """
+    ids = np.asarray(expert_ids)
+    w = np.asarray(topk_weights, dtype=np.float32)
+    x = np.asarray(x, dtype=np.float64)
+    dy32 = np.asarray(dy, dtype=np.float32)
+    dyb = bf16_round(dy32) if bf16_operands else dy32.astype(np.float64)
+    T, K = x.shape
+    E, N = W.shape[0], W.shape[1]
+    k = ids.shape[1]
+    dx = np.zeros((T, K))
+    dW = np.zeros((E, N, K))
+    dtopk = np.zeros((T, k))
+    for j in range(k):
+        for e in range(E):
+            t = np.nonzero(ids[:, j] == e)[0]
+            if t.size == 0:
+                continue
+            We = np.asarray(W[e], dtype=np.float64)
+            P = x[t] @ We.T                                   # unweighted product [m, N]
+            dtopk[t, j] = np.sum(dyb[t] * P, axis=1)
+            dx[t] += w[t, j].astype(np.float64)[:, None] * (dyb[t] @ We)
+            dW[e] += _dyw_operand(w[t, j], dy32[t], bf16_operands).T @ x[t]
+    return dx, dW, dtopk
+
+
+def moe_backward_rows(dy, x, W, expert_ids, topk_weights, tokens, bf16_operands=True):
+    """dx[tokens] and dtopk[tokens] by the same definitions as ``moe_backward``,
+    restricted to the given tokens (sampled checks at full size)."""
+    ids = np.asarray(expert_ids)
+    w = np.asarray(topk_weights, dtype=np.float32)
+    x = np.asarray(x, dtype=np.float64)
+    dy32 = np.asarray(dy, dtype=np.float32)
+    tok = np.asarray(tokens)
+    dyb = bf16_round(dy32[tok]) if bf16_operands else dy32[tok].astype(np.float64)
+    dx = np.zeros((tok.size, x.shape[1]))
+    dtopk = np.zeros((tok.size, ids.shape[1]))
+    for i, t in enumerate(tok):
+        for j in range(ids.shape[1]):
+            We = np.asarray(W[ids[t, j]], dtype=np.float64)
+            dtopk[i, j] = dyb[i] @ (We @ x[t])
+            dx[i] += np.float64(w[t, j]) * (dyb[i] @ We)
+    return dx, dtopk
+
+
+def moe_backward_dw_rows(dy, x, W, expert_ids, topk_weights, pairs, bf16_operands=True):
+    """dW[e, n, :] for the given (e, n) pairs, by the definition in
+    ``moe_backward`` (sum over expert e's assignments)."""
+    ids = np.asarray(expert_ids)
+    w = np.asarray(topk_weights, dtype=np.float32)
+    x = np.asarray(x, dtype=np.float64)
+    dy32 = np.asarray(dy, dtype=np.float32)
+    out = np.zeros((len(pairs), x.shape[1]))
+    for i, (e, n) in enumerate(pairs):
+        t, j = np.nonzero(ids == e)
+        if t.size == 0:
+            continue
+        a = _dyw_operand(w[t, j], dy32[t, n][:, None], bf16_operands)[:, 0]
+        out[i] = a @ x[t]
+    return out
+
+
+# --------------------------------------------------------------------------
+# Masked (fixed-capacity) decode layout  [P3 §5, "Masked" layout]
+# --------------------------------------------------------------------------
+def masked_grouped_gemm(x, W, masked_m, experts=None) -> np.ndarray:
+    """y[e, i, :] = x[e, i, :] W_e^T for i < masked_m[e].
+
+    Each expert reserves a fixed maximum of M rows and a mask marks the valid
+    ones [P3 §5].  Rows i >= masked_m[e] are not computed: they are returned
+    as NaN, meaning "not produced" (the GPU must leave them untouched).
+    ``W[e]`` may be anything numpy can widen to float64 [N, K]; ``experts``
+    restricts the work to a subset (the other experts are returned as NaN).
+    """
+    E, M_max = len(masked_m), x.shape[1]
+    N = np.asarray(W[0]).shape[0]
+    y = np.full((E, M_max, N), np.nan)
+    for e in (range(E) if experts is None else experts):
+        m = int(masked_m[e])
+        if m:
+            y[e, :m] = np.asarray(x[e, :m], dtype=np.float64) @ np.asarray(W[e], dtype=np.float64).T
+    return y
+
+
+# --------------------------------------------------------------------------
+# Error measures used by the parity bars
+# --------------------------------------------------------------------------
+def rel_frobenius(a, ref) -> float:
+    """||a - ref||_F / ||ref||_F (0 when both are zero)."""
+    a = np.asarray(a, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.linalg.norm(ref)
+    num = np.linalg.norm(a - ref)
+    return float(num / den) if den > 0 else float(num)
+
+
+def max_abs_ratio(a, ref) -> float:
+    """max|a - ref| / max|ref| (the bar is <= 2e-3 for bfloat16 inputs)."""
+    a = np.asarray(a, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.max(np.abs(ref)) if ref.size else 0.0
+    num = np.max(np.abs(a - ref)) if ref.size else 0.0
+    return float(num / den) if den > 0 else float(num)
