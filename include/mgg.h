@@ -1,0 +1,255 @@
+/*
+ * mgg.h - C ABI of the GB300 (sm_103a) MoE variable-size grouped GEMM.
+ *
+ * The operation: E expert problems Y_e = X_e W_e^T that share K (contraction)
+ * and N (output width) and differ only in their row count m_e, with
+ * sum_e m_e = T*k and empty experts legal ("Grouped GEMM", scholia-log, §1;
+ * "Grouped GEMM for MoE, in depth", §Problem descriptors and the tile
+ * scheduler).  The fused forward gathers token rows through a row->token map
+ * while loading and scatters each result, scaled by its routing weight and
+ * top-k combined, into its token's output row while storing
+ * ("grouped-gemm-moe", §How it works).  The backward, the bare grouped GEMM
+ * and the masked (fixed-capacity) decode layout are part of the same library
+ * ("Grouped GEMM for MoE, in depth", §The backward pass; "Grouped GEMM", §5).
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * - All tensor arguments are DEVICE pointers into memory the caller owns and
+ *   keeps alive until the stream work completes.  The library never
+ *   allocates, frees or synchronises; everything is enqueued on `stream`
+ *   (a cudaStream_t passed as void*, NULL = legacy default stream) in stream
+ *   order, so every call can be captured in a CUDA graph.
+ * - Layouts are dense row-major with the shapes given; no strides.
+ * - "bf16" tensors hold IEEE bfloat16 bit patterns (uint16); "f32" tensors
+ *   hold binary32.  Outputs are always f32 and are fully overwritten by the
+ *   call (the library zeroes them itself; see each entry point).
+ * - Host-checkable errors (null pointers, sizes, alignment, workspace size,
+ *   device architecture) are returned synchronously and nothing is launched.
+ *   Data-dependent errors (an expert id outside [0, E), non-monotone or
+ *   out-of-range offsets, a pipeline wait that ran out) cannot be seen by the
+ *   host without a sync: the kernels OR a bit into the caller's device word
+ *   *dev_status (int32, never cleared by the library) and keep every memory
+ *   access in bounds; the numerical results of that call are then
+ *   unspecified.
+ * - The bf16 tensor-core path needs K % 8 == 0 and N % 8 == 0 (16-byte rows
+ *   for TMA; "Grouped GEMM for MoE, in depth", §Data layout, offsets and
+ *   alignment) and 16-byte aligned base pointers.  The f32 path takes any
+ *   K, N >= 1 and 4-byte aligned pointers.
+ * - Only sm_103 devices are accepted (MGG_ERR_UNSUPPORTED_ARCH otherwise).
+ */
+#ifndef MGG_H
+#define MGG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MGG_OK = 0,
+  MGG_ERR_INVALID_ARG = 1,      /* null pointer, non-positive size, k > E, E too large */
+  MGG_ERR_ALIGNMENT = 2,        /* K or N not a multiple of 8 (bf16), misaligned pointer */
+  MGG_ERR_DTYPE = 3,            /* unknown dtype or layout */
+  MGG_ERR_WORKSPACE = 4,        /* ws_bytes smaller than mgg_workspace_bytes() */
+  MGG_ERR_UNSUPPORTED_ARCH = 5, /* current device is not sm_103 */
+  MGG_ERR_CUDA = 6              /* a CUDA runtime/driver call or launch failed */
+} mgg_status;
+
+typedef enum { MGG_BF16 = 0, MGG_F32 = 1 } mgg_dtype;
+
+typedef enum {
+  MGG_LAYOUT_CONTIGUOUS = 0,      /* rows grouped by expert + int32 end offsets */
+  MGG_LAYOUT_MASKED = 1,          /* [E, M_max, K] with per-expert valid row counts */
+  MGG_LAYOUT_CONTIGUOUS_SIZES = 2 /* rows grouped by expert + int32 group sizes */
+} mgg_layout;
+
+typedef enum {
+  MGG_OP_ROUTE = 0,
+  MGG_OP_FORWARD = 1,
+  MGG_OP_BACKWARD = 2,
+  MGG_OP_GROUPED_GEMM = 3,
+  MGG_OP_MASKED = 4
+} mgg_op;
+
+/* Bits the kernels OR into *dev_status. */
+#define MGG_DEV_BAD_EXPERT_ID 0x1 /* an expert id outside [0, E): assignment skipped */
+#define MGG_DEV_BAD_OFFSETS 0x2   /* end offsets decreasing / beyond rows, or masked_m > M_max */
+#define MGG_DEV_TIMEOUT 0x4       /* a pipeline wait exceeded its limit; the kernel gave up */
+
+/* Largest expert count the device router handles. */
+#define MGG_MAX_EXPERTS 1024
+
+/*
+ * Routing buffers (all device memory, caller-owned, S = T*k).  Filled by
+ * mgg_route / mgg_moe_forward; mgg_moe_backward reads them back (the saved
+ * context of the forward).
+ *   counts     [E]   int32  m_e, rows routed to expert e
+ *   end_offs   [E]   int32  inclusive prefix sums of counts (end offsets:
+ *                           counts [3,0,5] -> [3,3,8], "Grouped GEMM for MoE,
+ *                           in depth", §Data layout, offsets and alignment)
+ *   start      [E+1] int32  exclusive prefix sums; start[E] = S
+ *   tile_start [E+1] int32  exclusive prefix sums of the forward tile counts
+ *                           ceil(m_e/BM)*ceil(N/BN) ("Grouped GEMM for MoE,
+ *                           in depth", §Problem descriptors, pseudocode)
+ *   row_assign [S]   int32  sorted row r -> assignment a = t*k + j
+ *   row_token  [S]   int32  sorted row r -> token t
+ *   row_weight [S]   f32    sorted row r -> topk_weights[t, j]
+ */
+typedef struct {
+  int32_t* counts;
+  int32_t* end_offs;
+  int32_t* start;
+  int32_t* tile_start;
+  int32_t* row_assign;
+  int32_t* row_token;
+  float* row_weight;
+} mgg_routing;
+
+/* Human-readable name of a status code (static storage). */
+const char* mgg_status_string(mgg_status s);
+
+/*
+ * Tile shape the library uses for an op (BM rows x BN columns, BK contraction
+ * step), so callers can size schedules.  Returns MGG_ERR_DTYPE for an unknown
+ * op/dtype pair.  For MGG_OP_FORWARD the routing's tile_start counts tiles of
+ * this shape.
+ */
+mgg_status mgg_tile_config(mgg_op op, mgg_dtype dtype, int* BM, int* BN, int* BK);
+
+/*
+ * Bytes of scratch workspace `ws` an op needs (device memory, caller-owned,
+ * 256-byte aligned, contents need not be initialised and are clobbered).
+ * Arguments that an op does not use are ignored (pass 0).  Returns 0 for an
+ * invalid combination.
+ *   MGG_OP_ROUTE, MGG_OP_FORWARD : T, k, E
+ *   MGG_OP_BACKWARD              : T, k, E, N, K, dtype
+ *   MGG_OP_GROUPED_GEMM          : E
+ *   MGG_OP_MASKED                : 0 (no workspace)
+ */
+size_t mgg_workspace_bytes(mgg_op op, int T, int k, int E, int N, int K, mgg_dtype dtype);
+
+/*
+ * Device router: histogram, scans and a stable counting sort of the S = T*k
+ * assignments by expert, with no device-to-host sync ("grouped-gemm-moe",
+ * §How it works; "Grouped GEMM for MoE, in depth", §Problem descriptors,
+ * "the group sizes live on the device"; ties keep ascending a, as a stable
+ * argsort of the flattened ids, §Data layout).
+ *   expert_ids   [T, k] int32 (device)  expert of assignment (t, j)
+ *   topk_weights [T, k] f32   (device)  routing weight of (t, j)
+ *   N, dtype     output width and forward dtype, used only for
+ *                routing->tile_start (tile shape of mgg_tile_config(
+ *                MGG_OP_FORWARD, dtype))
+ *   routing      buffers to fill (see mgg_routing)
+ *   dev_status   [1] int32 (device): MGG_DEV_BAD_EXPERT_ID if an id is out
+ *                of range (that assignment is skipped)
+ *   ws, ws_bytes scratch of mgg_workspace_bytes(MGG_OP_ROUTE, T, k, E, ...)
+ * Errors: MGG_ERR_INVALID_ARG (null, T<1, k<1, E<1, E>MGG_MAX_EXPERTS,
+ * k>E is allowed: repeats are separate assignments), MGG_ERR_WORKSPACE,
+ * MGG_ERR_UNSUPPORTED_ARCH, MGG_ERR_CUDA.
+ */
+mgg_status mgg_route(const int32_t* expert_ids, const float* topk_weights, int T, int k, int E,
+                     int N, mgg_dtype dtype, const mgg_routing* routing, int32_t* dev_status, void* ws,
+                     size_t ws_bytes, void* stream);
+
+/*
+ * Bare variable-size grouped GEMM: the fused kernel with the permutation
+ * maps omitted, rows already grouped and written in order
+ * ("grouped-gemm-moe", §How it works, last paragraph; §Usage).
+ *
+ * MGG_LAYOUT_CONTIGUOUS:
+ *   A        [rows, K] (dtype)       rows grouped by expert
+ *   offs     [E] int32 END offsets   group e = rows offs[e-1] .. offs[e]-1;
+ *                                    must be non-decreasing with offs[E-1] == rows
+ *                                    (violations set MGG_DEV_BAD_OFFSETS and are
+ *                                    clamped into [previous, rows])
+ *   rows_or_Mmax = rows
+ *   C        [rows, N] f32           C[r] = A[r] W_e^T, every row written
+ * MGG_LAYOUT_CONTIGUOUS_SIZES: as CONTIGUOUS, but offs holds the group
+ *   sizes m_e ("grouped-gemm-moe", §Usage: group_sizes [200, 0, 500, 300]
+ *   for 1000 rows); the end offsets are their inclusive scan, formed on the
+ *   device (negative sizes set MGG_DEV_BAD_OFFSETS and count as 0)
+ * MGG_LAYOUT_MASKED ("Grouped GEMM", §5, masked layout for decode):
+ *   A        [E, M_max, K] (dtype)
+ *   offs     [E] int32 masked_m      valid rows per expert, 0..M_max (clamped;
+ *                                    larger values set MGG_DEV_BAD_OFFSETS)
+ *   rows_or_Mmax = M_max
+ *   C        [E, M_max, N] f32       C[e, i] = A[e, i] W_e^T for i < masked_m[e];
+ *                                    rows i >= masked_m[e] of A are never read and
+ *                                    rows of C are never written
+ * Both: W [E, N, K] (dtype) stored like nn.Linear.  ws: mgg_workspace_bytes
+ * (MGG_OP_GROUPED_GEMM or MGG_OP_MASKED).  Errors as for mgg_route plus
+ * MGG_ERR_ALIGNMENT and MGG_ERR_DTYPE.
+ */
+mgg_status mgg_grouped_gemm(const void* A, const void* W, float* C, mgg_dtype dtype,
+                            mgg_layout layout, const int32_t* offs, int rows_or_Mmax, int E,
+                            int N, int K, int32_t* dev_status, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/*
+ * Fused MoE forward: routes (as mgg_route) and runs one persistent grouped
+ * GEMM over all experts with gather-on-load and scale/scatter/combine-on-
+ * store ("grouped-gemm-moe", §How it works):
+ *   y[t, :] = sum_j topk_weights[t, j] * x[t, :] W_{expert_ids[t, j]}^T
+ *   x [T, K] (dtype), W [E, N, K] (dtype), expert_ids/topk_weights [T, k],
+ *   y [T, N] f32 (zeroed by the call, then accumulated atomically).
+ * routing receives the saved context for mgg_moe_backward.
+ * ws: mgg_workspace_bytes(MGG_OP_FORWARD, T, k, E, ...).
+ */
+mgg_status mgg_moe_forward(const void* x, const void* W, const int32_t* expert_ids,
+                           const float* topk_weights, int T, int K, int N, int E, int k,
+                           mgg_dtype dtype, float* y, const mgg_routing* routing,
+                           int32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Fused MoE backward of L = sum(dy * y) ("Grouped GEMM for MoE, in depth",
+ * §The backward pass; "grouped-gemm-moe", §How it works, backward):
+ *   dx    [T, K]    f32  dx[t] = sum_j w[t,j] * dy[t] W_e      (fused kernel,
+ *                        W read transposed, gather/scatter as in the forward)
+ *   dW    [E, N, K] f32  dW_e = sum_{a in e} (w_a dy[t(a)])^T x[t(a)]
+ *                        (per-expert A^T B over the jagged rows; an expert
+ *                        with no rows gets exactly +0)
+ *   dtopk [T, k]    f32  dtopk[t,j] = <dy[t], x[t] W_e^T>  (incoming gradient
+ *                        against the unweighted per-assignment product)
+ * On the bf16 path the tensor-core operands are bf16(dy) for dx and dtopk
+ * and bf16(fl32(w*dy)) for dW; the f32 path uses dy as given.  dx, dW and
+ * dtopk are overwritten.  routing must be the one filled by the forward of
+ * the same expert_ids/topk_weights.  ws: mgg_workspace_bytes(MGG_OP_BACKWARD,
+ * T, k, E, N, K, dtype).
+ */
+mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
+                            const mgg_routing* routing, int T, int K, int N, int E, int k,
+                            mgg_dtype dtype, float* dx, float* dW, float* dtopk,
+                            int32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Debug export of the device tile schedule: for every tile index tau of the
+ * forward's flat tile space, the values the GEMM kernel itself decodes
+ * (upper_bound on tile_start, column-block-major inside an expert,
+ * "Grouped GEMM for MoE, in depth", §Problem descriptors and the tile
+ * scheduler):  out[tau] = {e, mb, nb, row0, rows}  (int32 x 5).
+ * Entries tau >= routing->tile_start[E] are left untouched; max_tiles bounds
+ * the rows of `out` (entries beyond it are not written).
+ */
+mgg_status mgg_debug_tile_schedule(const mgg_routing* routing, int E, int N, mgg_dtype dtype,
+                                   int max_tiles, int32_t* out, void* stream);
+
+/*
+ * Benchmark instrumentation (no counterpart on the pages).  With n > 0,
+ * later calls record events[2*i] right before and events[2*i+1] right after
+ * the launch of their i-th main GEMM kernel, on the call's stream:
+ *   mgg_moe_forward        i = 0: fused gather/scatter GEMM
+ *   mgg_moe_backward       i = 0: dX (+ d routing weight), i = 1: dW
+ *   mgg_grouped_gemm       i = 0: bare or masked GEMM
+ * events are cudaEvent_t handles (created and destroyed by the caller) and
+ * must stay valid while set; n = 0 (or events = NULL) turns recording off.
+ * The setting is per host thread.  Returns MGG_ERR_INVALID_ARG for n < 0 or
+ * n > 8.
+ */
+mgg_status mgg_set_kernel_events(void* const* events, int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MGG_H */

@@ -1,0 +1,489 @@
+// C ABI of the library (declared in include/mgg.h): argument checks,
+// workspace carving, tensor-map encoding and stream-ordered launch
+// sequences.  Nothing here allocates, frees or synchronises.
+#include <stdlib.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/mgg.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace mgg {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int g_sms[kMaxDevices] = {};
+int g_arch_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
+
+bool current_device(int* dev) { return cudaGetDevice(dev) == cudaSuccess && *dev >= 0 && *dev < kMaxDevices; }
+
+mgg_status check_arch() {
+  int dev = 0;
+  if (!current_device(&dev)) return MGG_ERR_CUDA;
+  if (g_arch_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return MGG_ERR_CUDA;
+    g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return g_arch_ok[dev] == 1 ? MGG_OK : MGG_ERR_UNSUPPORTED_ARCH;
+}
+
+long long wait_limit() {
+  static long long lim = [] {
+    const char* s = getenv("MGG_WAIT_LIMIT");
+    const long long v = s ? atoll(s) : 0;
+    return v > 0 ? v : kDefaultWaitLimit;
+  }();
+  return lim;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+mgg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MGG_OK : MGG_ERR_CUDA; }
+
+// Benchmark instrumentation: event pairs recorded around the main GEMMs.
+thread_local cudaEvent_t t_events[16];
+thread_local int t_nevents = 0;
+
+void mark(int i, bool after, cudaStream_t st) {
+  if (2 * i + 1 < t_nevents) cudaEventRecord(t_events[2 * i + (after ? 1 : 0)], st);
+}
+
+// Launch one main GEMM between its instrumentation marks.
+template <typename F>
+cudaError_t timed(int i, cudaStream_t st, F&& launch) {
+  mark(i, false, st);
+  const cudaError_t e = launch();
+  mark(i, true, st);
+  return e;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Forward-path tile shape for a dtype.
+void rows_tile(mgg_dtype dt, int* BM, int* BN) {
+  if (dt == MGG_BF16) {
+    *BM = kRowsBM;
+    *BN = kRowsBN;
+  } else {
+    *BM = kSimtBM;
+    *BN = kSimtBN;
+  }
+}
+
+// bf16 weights [E][N][K] as a 3-D tensor map, box {64 along K, box_rows along N, 1}.
+bool tmap_weights(CUtensorMap* m, const void* W, int E, int N, int K, int box_inner,
+                  int box_rows) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                            static_cast<uint64_t>(E)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2};
+  const uint32_t box[3] = {static_cast<uint32_t>(box_inner), static_cast<uint32_t>(box_rows), 1};
+  return encode_tmap(m, W, 3, dims, strides, box);
+}
+
+struct BwdLayout {
+  size_t off_tile_start_dx, off_pstart, off_dy_b, off_dyw, total;
+  int S_pad_max;
+};
+
+BwdLayout bwd_layout(int T, int k, int E, int N, int K, mgg_dtype dt) {
+  (void)K;
+  BwdLayout L{};
+  const size_t S = static_cast<size_t>(T) * k;
+  size_t off = 0;
+  L.off_tile_start_dx = off;
+  off += round256((E + 1) * sizeof(int32_t));
+  L.off_pstart = off;
+  off += round256((E + 1) * sizeof(int32_t));
+  L.S_pad_max = 0;
+  if (dt == MGG_BF16) {
+    L.off_dy_b = off;
+    off += round256(static_cast<size_t>(T) * N * 2);
+    L.S_pad_max = static_cast<int>(S + static_cast<size_t>(kDwPad - 1) * E);
+    L.off_dyw = off;
+    off += round256(static_cast<size_t>(L.S_pad_max) * N * 2);
+  }
+  L.total = off;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+bool routing_ok(const mgg_routing* r) {
+  return r && r->counts && r->end_offs && r->start && r->tile_start && r->row_assign &&
+         r->row_token && r->row_weight;
+}
+
+mgg_status check_moe_sizes(int T, int K, int N, int E, int k, mgg_dtype dt) {
+  if (T < 1 || K < 1 || N < 1 || E < 1 || k < 1 || E > kMaxExperts) return MGG_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * k > (1LL << 30)) return MGG_ERR_INVALID_ARG;
+  if (dt != MGG_BF16 && dt != MGG_F32) return MGG_ERR_DTYPE;
+  if (dt == MGG_BF16 && (K % 8 != 0 || N % 8 != 0)) return MGG_ERR_ALIGNMENT;
+  return MGG_OK;
+}
+
+}  // namespace
+
+int num_sms() {
+  int dev = 0;
+  if (!current_device(&dev)) return 1;
+  if (g_sms[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = n > 0 ? n : 1;
+  }
+  return g_sms[dev];
+}
+
+bool encode_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tmap_encoder();
+  if (!fn) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) s[i] = strides_bytes[i];
+  const CUresult r =
+      fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+         const_cast<void*>(base), d, s, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace mgg
+
+using namespace mgg;
+
+extern "C" {
+
+const char* mgg_status_string(mgg_status s) {
+  switch (s) {
+    case MGG_OK: return "MGG_OK";
+    case MGG_ERR_INVALID_ARG: return "MGG_ERR_INVALID_ARG: null pointer or invalid size";
+    case MGG_ERR_ALIGNMENT: return "MGG_ERR_ALIGNMENT: K/N not a multiple of 8 or misaligned pointer";
+    case MGG_ERR_DTYPE: return "MGG_ERR_DTYPE: unknown dtype, layout or op";
+    case MGG_ERR_WORKSPACE: return "MGG_ERR_WORKSPACE: workspace too small or misaligned";
+    case MGG_ERR_UNSUPPORTED_ARCH: return "MGG_ERR_UNSUPPORTED_ARCH: current device is not sm_103";
+    case MGG_ERR_CUDA: return "MGG_ERR_CUDA: a CUDA call or kernel launch failed";
+  }
+  return "unknown mgg_status";
+}
+
+mgg_status mgg_tile_config(mgg_op op, mgg_dtype dtype, int* BM, int* BN, int* BK) {
+  if (!BM || !BN || !BK) return MGG_ERR_INVALID_ARG;
+  if (dtype != MGG_BF16 && dtype != MGG_F32) return MGG_ERR_DTYPE;
+  const bool bf = dtype == MGG_BF16;
+  switch (op) {
+    case MGG_OP_ROUTE:
+    case MGG_OP_FORWARD:
+    case MGG_OP_GROUPED_GEMM:
+      *BM = bf ? kRowsBM : kSimtBM;
+      *BN = bf ? kRowsBN : kSimtBN;
+      *BK = bf ? kBK : 16;
+      return MGG_OK;
+    case MGG_OP_BACKWARD:  // the dW tiles (dX uses the forward shape over K)
+      *BM = bf ? kDwBM : kSimtBM;
+      *BN = bf ? kDwBN : kSimtBN;
+      *BK = bf ? kDwPad : 16;
+      return MGG_OK;
+    case MGG_OP_MASKED:
+      *BM = bf ? kMaskedBM : kSimtBM;
+      *BN = bf ? kMaskedBI : kSimtBN;
+      *BK = bf ? kBK : 16;
+      return MGG_OK;
+  }
+  return MGG_ERR_DTYPE;
+}
+
+size_t mgg_workspace_bytes(mgg_op op, int T, int k, int E, int N, int K, mgg_dtype dtype) {
+  switch (op) {
+    case MGG_OP_ROUTE:
+    case MGG_OP_FORWARD:
+      if (T < 1 || k < 1 || E < 1 || E > kMaxExperts) return 0;
+      return route_ws_bytes(T, k, E);
+    case MGG_OP_BACKWARD:
+      if (T < 1 || k < 1 || E < 1 || E > kMaxExperts || N < 1 || K < 1) return 0;
+      if (dtype != MGG_BF16 && dtype != MGG_F32) return 0;
+      return bwd_layout(T, k, E, N, K, dtype).total;
+    case MGG_OP_GROUPED_GEMM:
+      if (E < 1 || E > kMaxExperts) return 0;
+      return 2 * round256((E + 1) * sizeof(int32_t));
+    case MGG_OP_MASKED:
+      return 0;
+  }
+  return 0;
+}
+
+mgg_status mgg_route(const int32_t* expert_ids, const float* topk_weights, int T, int k, int E,
+                     int N, mgg_dtype dtype, const mgg_routing* routing, int32_t* dev_status,
+                     void* ws, size_t ws_bytes, void* stream) {
+  if (!expert_ids || !topk_weights || !routing_ok(routing) || !dev_status || !ws)
+    return MGG_ERR_INVALID_ARG;
+  if (T < 1 || k < 1 || E < 1 || N < 1 || E > kMaxExperts) return MGG_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * k > (1LL << 30)) return MGG_ERR_INVALID_ARG;
+  if (dtype != MGG_BF16 && dtype != MGG_F32) return MGG_ERR_DTYPE;
+  if (ws_bytes < route_ws_bytes(T, k, E) || !aligned(ws, 256)) return MGG_ERR_WORKSPACE;
+  mgg_status s = check_arch();
+  if (s != MGG_OK) return s;
+  int BM, BN;
+  rows_tile(dtype, &BM, &BN);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return from_cuda(launch_route(expert_ids, topk_weights, T, k, E, BM, cdiv(N, BN),
+                                routing->counts, routing->end_offs, routing->start,
+                                routing->tile_start, routing->row_assign, routing->row_token,
+                                routing->row_weight, dev_status, ws, st));
+}
+
+mgg_status mgg_grouped_gemm(const void* A, const void* W, float* C, mgg_dtype dtype,
+                            mgg_layout layout, const int32_t* offs, int rows_or_Mmax, int E,
+                            int N, int K, int32_t* dev_status, void* ws, size_t ws_bytes,
+                            void* stream) {
+  if (!A || !W || !C || !offs || !dev_status) return MGG_ERR_INVALID_ARG;
+  if (rows_or_Mmax < 1 || E < 1 || N < 1 || K < 1 || E > kMaxExperts) return MGG_ERR_INVALID_ARG;
+  if (dtype != MGG_BF16 && dtype != MGG_F32) return MGG_ERR_DTYPE;
+  if (layout != MGG_LAYOUT_CONTIGUOUS && layout != MGG_LAYOUT_MASKED &&
+      layout != MGG_LAYOUT_CONTIGUOUS_SIZES)
+    return MGG_ERR_DTYPE;
+  const bool bf = dtype == MGG_BF16;
+  if (bf && (K % 8 != 0 || N % 8 != 0)) return MGG_ERR_ALIGNMENT;
+  if (!aligned(A, bf ? 16 : 4) || !aligned(W, bf ? 16 : 4) || !aligned(C, bf ? 16 : 4))
+    return MGG_ERR_ALIGNMENT;
+  mgg_status s = check_arch();
+  if (s != MGG_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  if (layout == MGG_LAYOUT_MASKED) {
+    if (rows_or_Mmax > 1 << 20) return MGG_ERR_INVALID_ARG;
+    MaskedParams p{A, offs, E, rows_or_Mmax, N, K, C, dev_status, wait_limit()};
+    if (!bf)
+      return from_cuda(timed(0, st, [&] { return launch_masked_f32(p, static_cast<const float*>(W), st); }));
+    CUtensorMap tm;
+    if (!tmap_weights(&tm, W, E, N, K, kBK, kMaskedBM)) return MGG_ERR_CUDA;
+    return from_cuda(timed(0, st, [&] { return launch_masked_gemm(tm, p, st); }));
+  }
+
+  const size_t need = mgg_workspace_bytes(MGG_OP_GROUPED_GEMM, 0, 0, E, N, K, dtype);
+  if (!ws || ws_bytes < need || !aligned(ws, 256)) return MGG_ERR_WORKSPACE;
+  int BM, BN;
+  rows_tile(dtype, &BM, &BN);
+  int32_t* start = at<int32_t>(ws, 0);
+  int32_t* tile_start = at<int32_t>(ws, round256((E + 1) * sizeof(int32_t)));
+  cudaError_t e = launch_offsets_scan(offs, layout == MGG_LAYOUT_CONTIGUOUS_SIZES, E, rows_or_Mmax,
+                                      BM, cdiv(N, BN), start, tile_start, dev_status, st);
+  if (e != cudaSuccess) return MGG_ERR_CUDA;
+  RowsParams p{};
+  p.A = A;
+  p.lda = K;
+  p.Kc = K;
+  p.row_token = nullptr;
+  p.tile_start = tile_start;
+  p.start = start;
+  p.E = E;
+  p.Nout = N;
+  p.out = C;
+  p.ldo = N;
+  p.dev_status = dev_status;
+  p.wait_limit = wait_limit();
+  if (!bf)
+    return from_cuda(timed(0, st, [&] {
+      return launch_rows_f32(kModeBare, false, p, static_cast<const float*>(W), K, st);
+    }));
+  CUtensorMap tm;
+  if (!tmap_weights(&tm, W, E, N, K, kBK, kRowsBN)) return MGG_ERR_CUDA;
+  return from_cuda(timed(0, st, [&] { return launch_rows_gemm(kModeBare, false, tm, p, st); }));
+}
+
+mgg_status mgg_moe_forward(const void* x, const void* W, const int32_t* expert_ids,
+                           const float* topk_weights, int T, int K, int N, int E, int k,
+                           mgg_dtype dtype, float* y, const mgg_routing* routing,
+                           int32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  if (!x || !W || !expert_ids || !topk_weights || !y || !routing_ok(routing) || !dev_status || !ws)
+    return MGG_ERR_INVALID_ARG;
+  mgg_status s = check_moe_sizes(T, K, N, E, k, dtype);
+  if (s != MGG_OK) return s;
+  const bool bf = dtype == MGG_BF16;
+  if (!aligned(x, bf ? 16 : 4) || !aligned(W, bf ? 16 : 4) || !aligned(y, bf ? 16 : 4))
+    return MGG_ERR_ALIGNMENT;
+  if (ws_bytes < route_ws_bytes(T, k, E) || !aligned(ws, 256)) return MGG_ERR_WORKSPACE;
+  s = check_arch();
+  if (s != MGG_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int BM, BN;
+  rows_tile(dtype, &BM, &BN);
+  cudaError_t e = launch_route(expert_ids, topk_weights, T, k, E, BM, cdiv(N, BN), routing->counts,
+                               routing->end_offs, routing->start, routing->tile_start,
+                               routing->row_assign, routing->row_token, routing->row_weight,
+                               dev_status, ws, st);
+  if (e != cudaSuccess) return MGG_ERR_CUDA;
+  if (cudaMemsetAsync(y, 0, static_cast<size_t>(T) * N * sizeof(float), st) != cudaSuccess)
+    return MGG_ERR_CUDA;
+  RowsParams p{};
+  p.A = x;
+  p.lda = K;
+  p.Kc = K;
+  p.row_token = routing->row_token;
+  p.row_weight = routing->row_weight;
+  p.tile_start = routing->tile_start;
+  p.start = routing->start;
+  p.E = E;
+  p.Nout = N;
+  p.out = y;
+  p.ldo = N;
+  p.dev_status = dev_status;
+  p.wait_limit = wait_limit();
+  if (!bf)
+    return from_cuda(timed(0, st, [&] {
+      return launch_rows_f32(kModeFused, false, p, static_cast<const float*>(W), K, st);
+    }));
+  CUtensorMap tm;
+  if (!tmap_weights(&tm, W, E, N, K, kBK, kRowsBN)) return MGG_ERR_CUDA;
+  return from_cuda(timed(0, st, [&] { return launch_rows_gemm(kModeFused, false, tm, p, st); }));
+}
+
+mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
+                            const mgg_routing* routing, int T, int K, int N, int E, int k,
+                            mgg_dtype dtype, float* dx, float* dW, float* dtopk,
+                            int32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  if (!dy || !x || !W || !routing_ok(routing) || !dx || !dW || !dtopk || !dev_status || !ws)
+    return MGG_ERR_INVALID_ARG;
+  mgg_status s = check_moe_sizes(T, K, N, E, k, dtype);
+  if (s != MGG_OK) return s;
+  const bool bf = dtype == MGG_BF16;
+  if (!aligned(x, bf ? 16 : 4) || !aligned(W, bf ? 16 : 4) || !aligned(dy, bf ? 16 : 4) ||
+      !aligned(dx, bf ? 16 : 4) || !aligned(dW, 4) || !aligned(dtopk, 4))
+    return MGG_ERR_ALIGNMENT;
+  const BwdLayout L = bwd_layout(T, k, E, N, K, dtype);
+  if (ws_bytes < L.total || !aligned(ws, 256)) return MGG_ERR_WORKSPACE;
+  s = check_arch();
+  if (s != MGG_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* tile_start_dx = at<int32_t>(ws, L.off_tile_start_dx);
+  int32_t* pstart = at<int32_t>(ws, L.off_pstart);
+  int BM, BN;
+  rows_tile(dtype, &BM, &BN);
+  if (launch_bwd_scan(routing->counts, E, BM, cdiv(K, BN), kDwPad, tile_start_dx, pstart, st) !=
+      cudaSuccess)
+    return MGG_ERR_CUDA;
+  if (cudaMemsetAsync(dx, 0, static_cast<size_t>(T) * K * sizeof(float), st) != cudaSuccess ||
+      cudaMemsetAsync(dtopk, 0, static_cast<size_t>(T) * k * sizeof(float), st) != cudaSuccess)
+    return MGG_ERR_CUDA;
+
+  RowsParams p{};
+  p.lda = N;
+  p.Kc = N;
+  p.row_token = routing->row_token;
+  p.row_weight = routing->row_weight;
+  p.row_assign = routing->row_assign;
+  p.tile_start = tile_start_dx;
+  p.start = routing->start;
+  p.E = E;
+  p.Nout = K;
+  p.out = dx;
+  p.ldo = K;
+  p.xdot = x;
+  p.ldx = K;
+  p.dtopk = dtopk;
+  p.dev_status = dev_status;
+  p.wait_limit = wait_limit();
+
+  DwParams q{};
+  q.x = x;
+  q.K = K;
+  q.N = N;
+  q.counts = routing->counts;
+  q.start = routing->start;
+  q.pstart = pstart;
+  q.row_token = routing->row_token;
+  q.row_weight = routing->row_weight;
+  q.dy = dy;
+  q.E = E;
+  q.dW = dW;
+  q.dev_status = dev_status;
+  q.wait_limit = wait_limit();
+
+  if (!bf) {
+    p.A = dy;
+    cudaError_t e = timed(0, st, [&] {
+      return launch_rows_f32(kModeFusedDtopk, true, p, static_cast<const float*>(W), K, st);
+    });
+    if (e != cudaSuccess) return MGG_ERR_CUDA;
+    return from_cuda(timed(1, st, [&] { return launch_dw_f32(q, st); }));
+  }
+
+  void* dy_b = at<void>(ws, L.off_dy_b);
+  void* dyw = at<void>(ws, L.off_dyw);
+  if (launch_bwd_prep(dy, T, N, routing->counts, routing->start, pstart, routing->row_token,
+                      routing->row_weight, E, L.S_pad_max, dy_b, dyw, st) != cudaSuccess)
+    return MGG_ERR_CUDA;
+  p.A = dy_b;
+  CUtensorMap tm_wt;
+  if (!tmap_weights(&tm_wt, W, E, N, K, 64, 64)) return MGG_ERR_CUDA;
+  if (timed(0, st, [&] { return launch_rows_gemm(kModeFusedDtopk, true, tm_wt, p, st); }) !=
+      cudaSuccess)
+    return MGG_ERR_CUDA;
+
+  q.dyw = dyw;
+  CUtensorMap tm_dyw;
+  const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(L.S_pad_max)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(N) * 2};
+  const uint32_t box[2] = {64, static_cast<uint32_t>(kDwPad)};
+  if (!encode_tmap(&tm_dyw, dyw, 2, dims, strides, box)) return MGG_ERR_CUDA;
+  return from_cuda(timed(1, st, [&] { return launch_dw_gemm(tm_dyw, q, st); }));
+}
+
+mgg_status mgg_debug_tile_schedule(const mgg_routing* routing, int E, int N, mgg_dtype dtype,
+                                   int max_tiles, int32_t* out, void* stream) {
+  if (!routing || !routing->tile_start || !routing->start || !out) return MGG_ERR_INVALID_ARG;
+  if (E < 1 || E > kMaxExperts || N < 1 || max_tiles < 0) return MGG_ERR_INVALID_ARG;
+  if (dtype != MGG_BF16 && dtype != MGG_F32) return MGG_ERR_DTYPE;
+  mgg_status s = check_arch();
+  if (s != MGG_OK) return s;
+  int BM, BN;
+  rows_tile(dtype, &BM, &BN);
+  (void)BN;
+  return from_cuda(launch_debug_schedule(routing->tile_start, routing->start, E, BM, max_tiles, out,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+mgg_status mgg_set_kernel_events(void* const* events, int n) {
+  if (n < 0 || n > 8) return MGG_ERR_INVALID_ARG;
+  if (!events || n == 0) {
+    t_nevents = 0;
+    return MGG_OK;
+  }
+  for (int i = 0; i < 2 * n; ++i) t_events[i] = static_cast<cudaEvent_t>(events[i]);
+  t_nevents = 2 * n;
+  return MGG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,117 @@
+// Host-side interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mgg {
+
+// Tile shapes of the tensor-core kernels.
+constexpr int kRowsBM = 128;   // rows (assignments) per tile: MMA M
+constexpr int kRowsBN = 256;   // output columns per tile: MMA N
+constexpr int kBK = 64;        // contraction step: one 128-byte swizzle row of bf16
+constexpr int kDwBM = 128;     // dW tile: K-output rows (MMA M)
+constexpr int kDwBN = 256;     // dW tile: N-output columns (MMA N)
+constexpr int kDwPad = 64;     // expert segments of the scaled dY operand are padded to this
+constexpr int kMaskedBM = 128; // decode tile: weight rows (MMA M)
+constexpr int kMaskedBI = 64;  // decode tile: activation rows per tile (MMA N <= 64)
+constexpr int kSimtBM = 64;    // f32 path tile rows
+constexpr int kSimtBN = 64;    // f32 path tile columns
+constexpr int kRouteChunk = 256;
+constexpr int kMaxExperts = 1024;
+
+// Default pipeline wait limit in SM clock cycles (about a second).
+constexpr long long kDefaultWaitLimit = 2000000000LL;
+
+enum RowsMode { kModeBare = 0, kModeFused = 1, kModeFusedDtopk = 2 };
+
+// One launch of the row-gathering grouped GEMM (forward, bare, dX).
+struct RowsParams {
+  const void* A;               // [*, lda] rows, gathered through row_token (or identity)
+  int lda;                     // elements per A row
+  int Kc;                      // contraction length
+  const int32_t* row_token;    // [S] sorted row -> A row; null = identity (bare)
+  const float* row_weight;     // [S] fused: per-row scale
+  const int32_t* row_assign;   // [S] dtopk: sorted row -> assignment
+  const int32_t* tile_start;   // [E+1]
+  const int32_t* start;        // [E+1]
+  int E;
+  int Nout;                    // output columns
+  float* out;                  // bare: [rows, Nout]; fused: [T, Nout] accumulated
+  int ldo;
+  const void* xdot;            // dtopk: x [T, ldx] (same dtype as A)
+  int ldx;
+  float* dtopk;                // dtopk: [S] indexed by assignment
+  int32_t* dev_status;
+  long long wait_limit;
+};
+
+struct DwParams {
+  const void* x;               // [T, K]
+  int K;
+  int N;
+  const void* dyw;             // [S_pad, N] scaled sorted dY, expert segments padded
+  const int32_t* counts;       // [E]
+  const int32_t* start;        // [E+1]
+  const int32_t* pstart;       // [E+1] padded segment starts
+  const int32_t* row_token;    // [S]
+  const float* row_weight;     // [S] (f32 path)
+  const float* dy;             // [T, N] (f32 path)
+  int E;
+  float* dW;                   // [E, N, K]
+  int32_t* dev_status;
+  long long wait_limit;
+};
+
+struct MaskedParams {
+  const void* x;               // [E, M_max, K]
+  const int32_t* masked_m;     // [E]
+  int E, M_max, N, K;
+  float* y;                    // [E, M_max, N]
+  int32_t* dev_status;
+  long long wait_limit;
+};
+
+// device properties
+int num_sms();
+
+// tensor maps
+bool encode_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box);
+
+// router.cu
+cudaError_t launch_route(const int32_t* ids, const float* w, int T, int k, int E, int BM,
+                         int tiles_n, int32_t* counts, int32_t* end_offs, int32_t* start,
+                         int32_t* tile_start, int32_t* row_assign, int32_t* row_token,
+                         float* row_weight, int32_t* dev_status, void* ws, cudaStream_t st);
+size_t route_ws_bytes(int T, int k, int E);
+cudaError_t launch_offsets_scan(const int32_t* offs, bool is_sizes, int E, int rows, int BM,
+                                int tiles_n, int32_t* start, int32_t* tile_start,
+                                int32_t* dev_status, cudaStream_t st);
+cudaError_t launch_bwd_scan(const int32_t* counts, int E, int BM, int tiles_n, int pad,
+                            int32_t* tile_start_dx, int32_t* pstart, cudaStream_t st);
+cudaError_t launch_bwd_prep(const float* dy, int T, int N, const int32_t* counts,
+                            const int32_t* start, const int32_t* pstart, const int32_t* row_token,
+                            const float* row_weight, int E, int S_pad_max, void* dy_b, void* dyw,
+                            cudaStream_t st);
+cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* start, int E, int BM,
+                                  int max_tiles, int32_t* out, cudaStream_t st);
+
+// gemm_rows.cu (tcgen05)
+cudaError_t launch_rows_gemm(int mode, bool b_mn_major, const CUtensorMap& tmap_b,
+                             const RowsParams& p, cudaStream_t st);
+// gemm_dw.cu (tcgen05)
+cudaError_t launch_dw_gemm(const CUtensorMap& tmap_dyw, const DwParams& p, cudaStream_t st);
+// gemm_masked.cu (tcgen05)
+cudaError_t launch_masked_gemm(const CUtensorMap& tmap_w, const MaskedParams& p, cudaStream_t st);
+
+// simt_f32.cu (exact f32 path)
+cudaError_t launch_rows_f32(int mode, bool w_transposed, const RowsParams& p, const float* W,
+                            int Kw, cudaStream_t st);
+cudaError_t launch_dw_f32(const DwParams& p, cudaStream_t st);
+cudaError_t launch_masked_f32(const MaskedParams& p, const float* W, cudaStream_t st);
+
+}  // namespace mgg

@@ -1,0 +1,332 @@
+// Device router and the small prep kernels around the grouped GEMMs.
+//
+// Routing turns the S = T*k token->expert assignments into a sort by expert:
+// per-expert counts, end offsets, exclusive starts, a row->token map and a
+// per-row routing weight ("grouped-gemm-moe", §How it works), plus the
+// per-expert tile prefix sums of the persistent GEMM ("Grouped GEMM for MoE,
+// in depth", §Problem descriptors and the tile scheduler).  All of it runs on
+// the device with no host read-back, so the layer stays graph-capturable
+// (same page, "the group sizes live on the device").  The permutation is a
+// stable counting sort: ties keep ascending assignment index a = t*k + j,
+// the order a stable argsort of the flattened ids gives (same page, §Data
+// layout, offsets and alignment).
+#include "internal.h"
+#include "schedule.cuh"
+
+namespace mgg {
+
+namespace {
+
+constexpr int kScanThreads = 1024;
+
+// Exclusive scan of one int per thread over the whole block (blockDim.x a
+// multiple of 32, at most 1024).  *total receives the block sum.
+template <typename Op>
+__device__ int block_scan_excl(int v, int identity, Op op, int* total) {
+  __shared__ int warp_acc[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x = op(x, y);
+  }
+  // exclusive within the warp
+  int ex = __shfl_up_sync(0xffffffffu, x, 1);
+  if (lane == 0) ex = identity;
+  if (lane == 31) warp_acc[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int s = lane < nw ? warp_acc[lane] : identity;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s = op(s, y);
+    }
+    warp_acc[lane] = s;  // inclusive over warps
+  }
+  __syncthreads();
+  const int res = wid > 0 ? op(warp_acc[wid - 1], ex) : ex;
+  *total = warp_acc[nw - 1];
+  __syncthreads();
+  return res;
+}
+
+struct AddOp {
+  __device__ int operator()(int a, int b) const { return a + b; }
+};
+struct MaxOp {
+  __device__ int operator()(int a, int b) const { return a > b ? a : b; }
+};
+
+// Per-chunk expert histogram (chunk = kRouteChunk consecutive assignments).
+__global__ void route_hist_kernel(const int32_t* __restrict__ ids, int S, int E,
+                                  int32_t* __restrict__ chunk_hist, int32_t* dev_status) {
+  __shared__ int h[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
+  __syncthreads();
+  const int a = blockIdx.x * kRouteChunk + threadIdx.x;
+  if (a < S) {
+    const int id = ids[a];
+    if (id >= 0 && id < E)
+      atomicAdd(&h[id], 1);
+    else
+      atomicOr(dev_status, kDevBadExpertId);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    chunk_hist[static_cast<size_t>(blockIdx.x) * E + e] = h[e];
+}
+
+// One block: counts, offsets, tile prefix sums; then rewrites chunk_hist into
+// each chunk's first output row per expert.
+__global__ void route_scan_kernel(int32_t* __restrict__ chunk_hist, int nchunks, int E, int BM,
+                                  int tiles_n, int32_t* __restrict__ counts,
+                                  int32_t* __restrict__ end_offs, int32_t* __restrict__ start,
+                                  int32_t* __restrict__ tile_start) {
+  const int e = threadIdx.x;
+  int m = 0;
+  if (e < E)
+    for (int c = 0; c < nchunks; ++c) m += chunk_hist[static_cast<size_t>(c) * E + e];
+  int total_rows, total_tiles;
+  const int st = block_scan_excl(m, 0, AddOp(), &total_rows);
+  const int tiles = e < E ? cdiv(m, BM) * tiles_n : 0;
+  const int ts = block_scan_excl(tiles, 0, AddOp(), &total_tiles);
+  if (e < E) {
+    counts[e] = m;
+    start[e] = st;
+    end_offs[e] = st + m;
+    tile_start[e] = ts;
+    int run = st;
+    for (int c = 0; c < nchunks; ++c) {
+      const size_t i = static_cast<size_t>(c) * E + e;
+      const int h = chunk_hist[i];
+      chunk_hist[i] = run;
+      run += h;
+    }
+  }
+  if (e == 0) {
+    start[E] = total_rows;
+    tile_start[E] = total_tiles;
+  }
+}
+
+// Stable scatter: rank of an assignment among the earlier assignments of its
+// chunk with the same expert, plus that chunk's first row for the expert.
+__global__ void route_scatter_kernel(const int32_t* __restrict__ ids,
+                                     const float* __restrict__ w, int S, int k, int E,
+                                     const int32_t* __restrict__ chunk_first,
+                                     int32_t* __restrict__ row_assign,
+                                     int32_t* __restrict__ row_token,
+                                     float* __restrict__ row_weight) {
+  __shared__ int sid[kRouteChunk];
+  const int a = blockIdx.x * kRouteChunk + threadIdx.x;
+  const int id = a < S ? ids[a] : -1;
+  sid[threadIdx.x] = id;
+  __syncthreads();
+  if (a < S && id >= 0 && id < E) {
+    int rank = 0;
+    for (int i = 0; i < static_cast<int>(threadIdx.x); ++i) rank += (sid[i] == id);
+    const int r = chunk_first[static_cast<size_t>(blockIdx.x) * E + id] + rank;
+    row_assign[r] = a;
+    row_token[r] = a / k;
+    row_weight[r] = w[a];
+  }
+}
+
+// Bare layout: caller's end offsets (or group sizes, scanned here) ->
+// clamped starts and tile prefix sums.  Offsets are made non-decreasing and
+// kept within [0, rows] so that every access stays in bounds; any repair is
+// reported.
+__global__ void offsets_scan_kernel(const int32_t* __restrict__ offs, int is_sizes, int E,
+                                    int rows, int BM, int tiles_n, int32_t* __restrict__ start,
+                                    int32_t* __restrict__ tile_start, int32_t* dev_status) {
+  const int e = threadIdx.x;
+  int raw = e < E ? offs[e] : 0;
+  bool bad = false;
+  if (is_sizes) {
+    bad = e < E && raw < 0;
+    int tot;
+    const int size = e < E ? max(raw, 0) : 0;
+    raw = block_scan_excl(size, 0, AddOp(), &tot) + size;  // inclusive: end offset
+  }
+  int run_max_total;
+  const int prev_max = block_scan_excl(e < E ? max(raw, 0) : 0, 0, MaxOp(), &run_max_total);
+  const int end_c = e < E ? min(rows, max(prev_max, raw)) : 0;
+  const int prev_c = min(rows, prev_max);
+  bad = bad || ((e < E) && (raw < prev_max || raw > rows || raw < 0 || (e == E - 1 && raw != rows)));
+  if (bad) atomicOr(dev_status, kDevBadOffsets);
+  const int m = e < E ? end_c - prev_c : 0;
+  int total_tiles;
+  const int ts = block_scan_excl(e < E ? cdiv(m, BM) * tiles_n : 0, 0, AddOp(), &total_tiles);
+  if (e < E) {
+    start[e] = prev_c;
+    tile_start[e] = ts;
+    if (e == E - 1) {
+      start[E] = end_c;
+      tile_start[E] = total_tiles;
+    }
+  }
+}
+
+// Backward schedules from the forward's counts: dX tile prefix sums and the
+// padded segment starts of the scaled dY operand of dW.
+__global__ void bwd_scan_kernel(const int32_t* __restrict__ counts, int E, int BM, int tiles_n,
+                                int pad, int32_t* __restrict__ tile_start_dx,
+                                int32_t* __restrict__ pstart) {
+  const int e = threadIdx.x;
+  const int m = e < E ? counts[e] : 0;
+  int total_tiles, total_pad;
+  const int ts = block_scan_excl(e < E ? cdiv(m, BM) * tiles_n : 0, 0, AddOp(), &total_tiles);
+  const int ps = block_scan_excl(e < E ? cdiv(m, pad) * pad : 0, 0, AddOp(), &total_pad);
+  if (e < E) {
+    tile_start_dx[e] = ts;
+    pstart[e] = ps;
+  }
+  if (e == 0) {
+    tile_start_dx[E] = total_tiles;
+    pstart[E] = total_pad;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat16 a = __float2bfloat16_rn(lo);
+  const __nv_bfloat16 b = __float2bfloat16_rn(hi);
+  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+}
+
+// dy_b = bf16(dy), 8 elements per thread (N % 8 == 0).
+__global__ void cast_bf16_kernel(const float* __restrict__ src, uint4* __restrict__ dst,
+                                 size_t n8) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(src)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(src)[2 * i + 1];
+    uint4 o;
+    o.x = pack_bf16x2(a.x, a.y);
+    o.y = pack_bf16x2(a.z, a.w);
+    o.z = pack_bf16x2(b.x, b.y);
+    o.w = pack_bf16x2(b.z, b.w);
+    dst[i] = o;
+  }
+}
+
+// Scaled, expert-sorted dY for dW: padded row p of expert e holds
+// bf16(fl32(w_r * dy[token_r])) for its sorted row r, or zeros in the
+// padding.  One block per padded row.
+__global__ void dyw_prep_kernel(const float* __restrict__ dy, int N,
+                                const int32_t* __restrict__ counts,
+                                const int32_t* __restrict__ start,
+                                const int32_t* __restrict__ pstart,
+                                const int32_t* __restrict__ row_token,
+                                const float* __restrict__ row_weight, int E,
+                                uint4* __restrict__ dyw) {
+  const int p = blockIdx.x;
+  if (p >= __ldg(pstart + E)) return;
+  int lo = 0, hi = E + 1;  // expert whose padded segment holds p
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(pstart + mid) > p)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  const int e = lo - 1;
+  const int local = p - __ldg(pstart + e);
+  const int n8 = N / 8;
+  uint4* out = dyw + static_cast<size_t>(p) * n8;
+  if (local >= __ldg(counts + e)) {
+    for (int i = threadIdx.x; i < n8; i += blockDim.x) out[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const int r = __ldg(start + e) + local;
+  const float wr = __ldg(row_weight + r);
+  const float4* src = reinterpret_cast<const float4*>(dy + static_cast<size_t>(__ldg(row_token + r)) * N);
+  for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+    const float4 a = src[2 * i];
+    const float4 b = src[2 * i + 1];
+    uint4 o;
+    o.x = pack_bf16x2(__fmul_rn(wr, a.x), __fmul_rn(wr, a.y));
+    o.y = pack_bf16x2(__fmul_rn(wr, a.z), __fmul_rn(wr, a.w));
+    o.z = pack_bf16x2(__fmul_rn(wr, b.x), __fmul_rn(wr, b.y));
+    o.w = pack_bf16x2(__fmul_rn(wr, b.z), __fmul_rn(wr, b.w));
+    out[i] = o;
+  }
+}
+
+__global__ void debug_schedule_kernel(const int32_t* __restrict__ tile_start,
+                                      const int32_t* __restrict__ start, int E, int BM,
+                                      int max_tiles, int32_t* __restrict__ out) {
+  const int total = min(__ldg(tile_start + E), max_tiles);
+  for (int tau = blockIdx.x * blockDim.x + threadIdx.x; tau < total;
+       tau += gridDim.x * blockDim.x) {
+    const Tile t = decode_tile(tau, tile_start, start, E, BM);
+    int32_t* o = out + static_cast<size_t>(tau) * 5;
+    o[0] = t.e;
+    o[1] = t.mb;
+    o[2] = t.nb;
+    o[3] = t.row0;
+    o[4] = t.rows;
+  }
+}
+
+}  // namespace
+
+size_t route_ws_bytes(int T, int k, int E) {
+  const size_t S = static_cast<size_t>(T) * k;
+  const size_t nchunks = (S + kRouteChunk - 1) / kRouteChunk;
+  return ((nchunks * E * sizeof(int32_t)) + 255) / 256 * 256;
+}
+
+cudaError_t launch_route(const int32_t* ids, const float* w, int T, int k, int E, int BM,
+                         int tiles_n, int32_t* counts, int32_t* end_offs, int32_t* start,
+                         int32_t* tile_start, int32_t* row_assign, int32_t* row_token,
+                         float* row_weight, int32_t* dev_status, void* ws, cudaStream_t st) {
+  const int S = T * k;
+  const int nchunks = (S + kRouteChunk - 1) / kRouteChunk;
+  int32_t* chunk = static_cast<int32_t*>(ws);
+  route_hist_kernel<<<nchunks, kRouteChunk, 0, st>>>(ids, S, E, chunk, dev_status);
+  route_scan_kernel<<<1, kScanThreads, 0, st>>>(chunk, nchunks, E, BM, tiles_n, counts,
+                                                end_offs, start, tile_start);
+  route_scatter_kernel<<<nchunks, kRouteChunk, 0, st>>>(ids, w, S, k, E, chunk, row_assign,
+                                                        row_token, row_weight);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_offsets_scan(const int32_t* offs, bool is_sizes, int E, int rows, int BM,
+                                int tiles_n, int32_t* start, int32_t* tile_start,
+                                int32_t* dev_status, cudaStream_t st) {
+  offsets_scan_kernel<<<1, kScanThreads, 0, st>>>(offs, is_sizes ? 1 : 0, E, rows, BM, tiles_n,
+                                                  start, tile_start, dev_status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_scan(const int32_t* counts, int E, int BM, int tiles_n, int pad,
+                            int32_t* tile_start_dx, int32_t* pstart, cudaStream_t st) {
+  bwd_scan_kernel<<<1, kScanThreads, 0, st>>>(counts, E, BM, tiles_n, pad, tile_start_dx, pstart);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prep(const float* dy, int T, int N, const int32_t* counts,
+                            const int32_t* start, const int32_t* pstart, const int32_t* row_token,
+                            const float* row_weight, int E, int S_pad_max, void* dy_b, void* dyw,
+                            cudaStream_t st) {
+  const size_t n8 = static_cast<size_t>(T) * N / 8;
+  const int blocks = static_cast<int>(std::min<size_t>((n8 + 255) / 256, 65536));
+  cast_bf16_kernel<<<blocks, 256, 0, st>>>(dy, static_cast<uint4*>(dy_b), n8);
+  if (S_pad_max > 0)
+    dyw_prep_kernel<<<S_pad_max, 256, 0, st>>>(dy, N, counts, start, pstart, row_token,
+                                               row_weight, E, static_cast<uint4*>(dyw));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* start, int E, int BM,
+                                  int max_tiles, int32_t* out, cudaStream_t st) {
+  if (max_tiles <= 0) return cudaSuccess;
+  const int blocks = std::min((max_tiles + 255) / 256, 4096);
+  debug_schedule_kernel<<<blocks, 256, 0, st>>>(tile_start, start, E, BM, max_tiles, out);
+  return cudaGetLastError();
+}
+
+}  // namespace mgg

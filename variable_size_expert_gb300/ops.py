@@ -1,0 +1,258 @@
+"""torch-facing API over the C ABI.
+
+PyTorch supplies device memory and the current stream; every step of the
+method runs in libmgg.so's kernels.  Inputs must be CUDA tensors on an
+sm_103 device; there is no CPU fallback.
+
+Functions mirror the pages' usage ("grouped-gemm-moe", §Usage):
+  moe(x, W, expert_ids, topk_weights)        differentiable fused MoE layer
+  grouped_gemm(a, W, group_sizes | end_offs) bare variable-size grouped GEMM
+plus the lower-level calls (route, moe_forward, moe_backward,
+grouped_gemm_masked, debug_tile_schedule).
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib as L
+
+__all__ = [
+    "RoutingBuffers", "route", "moe_forward", "moe_backward", "moe", "grouped_gemm",
+    "grouped_gemm_masked", "debug_tile_schedule", "tile_config", "workspace_bytes",
+    "new_status", "read_status",
+]
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return L.MGG_BF16
+    if t.dtype == torch.float32:
+        return L.MGG_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: bfloat16 or float32")
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def new_status(device) -> torch.Tensor:
+    """A zeroed device status word (int32[1]) for the kernels to OR error bits into."""
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def read_status(status: torch.Tensor) -> int:
+    """Synchronising read of a status word (for tests and debugging)."""
+    return int(status.item())
+
+
+def tile_config(op: int, dtype: torch.dtype = torch.bfloat16):
+    lib = L.load()
+    bm, bn, bk = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    code = L.MGG_BF16 if dtype == torch.bfloat16 else L.MGG_F32
+    L.check(lib.mgg_tile_config(op, code, ctypes.byref(bm), ctypes.byref(bn), ctypes.byref(bk)),
+            "mgg_tile_config")
+    return bm.value, bn.value, bk.value
+
+
+def workspace_bytes(op: int, T=0, k=0, E=0, N=0, K=0, dtype=torch.bfloat16) -> int:
+    code = L.MGG_BF16 if dtype == torch.bfloat16 else L.MGG_F32
+    return int(L.load().mgg_workspace_bytes(op, T, k, E, N, K, code))
+
+
+@dataclass
+class RoutingBuffers:
+    """Device routing buffers (see mgg_routing in include/mgg.h)."""
+    counts: torch.Tensor
+    end_offs: torch.Tensor
+    start: torch.Tensor
+    tile_start: torch.Tensor
+    row_assign: torch.Tensor
+    row_token: torch.Tensor
+    row_weight: torch.Tensor
+
+    @staticmethod
+    def empty(T: int, k: int, E: int, device) -> "RoutingBuffers":
+        S = T * k
+        i32 = dict(dtype=torch.int32, device=device)
+        return RoutingBuffers(
+            counts=torch.empty(E, **i32), end_offs=torch.empty(E, **i32),
+            start=torch.empty(E + 1, **i32), tile_start=torch.empty(E + 1, **i32),
+            row_assign=torch.empty(S, **i32), row_token=torch.empty(S, **i32),
+            row_weight=torch.empty(S, dtype=torch.float32, device=device))
+
+    def struct(self) -> L.Routing:
+        return L.Routing(*(_ptr(getattr(self, f)) for f, _ in L.Routing._fields_))
+
+
+def _ids_i32(expert_ids: torch.Tensor) -> torch.Tensor:
+    # the ABI takes int32 ids; torch's usual int64 is narrowed here (marshalling)
+    return expert_ids if expert_ids.dtype == torch.int32 else expert_ids.to(torch.int32)
+
+
+def route(expert_ids: torch.Tensor, topk_weights: torch.Tensor, E: int, N: int,
+          dtype: torch.dtype = torch.bfloat16, status: torch.Tensor | None = None,
+          out: RoutingBuffers | None = None) -> RoutingBuffers:
+    """Device routing: counts, offsets, stable permutation, tile prefix sums."""
+    lib = L.load()
+    ids = _ids_i32(expert_ids).contiguous()
+    w = topk_weights.contiguous().float()
+    T, k = ids.shape
+    dev = ids.device
+    r = out or RoutingBuffers.empty(T, k, E, dev)
+    st = status if status is not None else new_status(dev)
+    code = L.MGG_BF16 if dtype == torch.bfloat16 else L.MGG_F32
+    nbytes = lib.mgg_workspace_bytes(L.MGG_OP_ROUTE, T, k, E, N, 0, code)
+    ws = _workspace(nbytes, dev)
+    rs = r.struct()
+    L.check(lib.mgg_route(_ptr(ids), _ptr(w), T, k, E, N, code, ctypes.byref(rs), _ptr(st),
+                          _ptr(ws), ws.numel(), _stream()), "mgg_route")
+    return r
+
+
+def moe_forward(x: torch.Tensor, W: torch.Tensor, expert_ids: torch.Tensor,
+                topk_weights: torch.Tensor, status: torch.Tensor | None = None,
+                out: torch.Tensor | None = None, routing: RoutingBuffers | None = None,
+                workspace: torch.Tensor | None = None):
+    """Fused MoE forward.  Returns (y [T, N] float32, routing)."""
+    lib = L.load()
+    code = _dtype_code(x)
+    if W.dtype != x.dtype:
+        raise TypeError("x and W must share a dtype")
+    T, K = x.shape
+    E, N, K2 = W.shape
+    if K2 != K:
+        raise ValueError("W must be [E, N, K] with the K of x")
+    ids = _ids_i32(expert_ids).contiguous()
+    w = topk_weights.detach().contiguous().float()
+    k = ids.shape[1]
+    dev = x.device
+    y = out if out is not None else torch.empty(T, N, dtype=torch.float32, device=dev)
+    r = routing or RoutingBuffers.empty(T, k, E, dev)
+    st = status if status is not None else new_status(dev)
+    nbytes = lib.mgg_workspace_bytes(L.MGG_OP_FORWARD, T, k, E, N, K, code)
+    ws = workspace if workspace is not None and workspace.numel() >= nbytes else _workspace(nbytes, dev)
+    rs = r.struct()
+    L.check(lib.mgg_moe_forward(_ptr(x), _ptr(W), _ptr(ids), _ptr(w), T, K, N, E, k, code,
+                                _ptr(y), ctypes.byref(rs), _ptr(st), _ptr(ws), ws.numel(),
+                                _stream()), "mgg_moe_forward")
+    return y, r
+
+
+def moe_backward(dy: torch.Tensor, x: torch.Tensor, W: torch.Tensor, routing: RoutingBuffers,
+                 k: int, status: torch.Tensor | None = None, dx=None, dW=None, dtopk=None,
+                 workspace: torch.Tensor | None = None):
+    """Fused MoE backward.  Returns (dx [T,K], dW [E,N,K], dtopk [T,k]), all float32."""
+    lib = L.load()
+    code = _dtype_code(x)
+    T, K = x.shape
+    E, N, _ = W.shape
+    dev = x.device
+    dy = dy.contiguous().float()
+    dx = dx if dx is not None else torch.empty(T, K, dtype=torch.float32, device=dev)
+    dW = dW if dW is not None else torch.empty(E, N, K, dtype=torch.float32, device=dev)
+    dtopk = dtopk if dtopk is not None else torch.empty(T, k, dtype=torch.float32, device=dev)
+    st = status if status is not None else new_status(dev)
+    nbytes = lib.mgg_workspace_bytes(L.MGG_OP_BACKWARD, T, k, E, N, K, code)
+    ws = workspace if workspace is not None and workspace.numel() >= nbytes else _workspace(nbytes, dev)
+    rs = routing.struct()
+    L.check(lib.mgg_moe_backward(_ptr(dy), _ptr(x), _ptr(W), ctypes.byref(rs), T, K, N, E, k, code,
+                                 _ptr(dx), _ptr(dW), _ptr(dtopk), _ptr(st), _ptr(ws), ws.numel(),
+                                 _stream()), "mgg_moe_backward")
+    return dx, dW, dtopk
+
+
+class _MoEFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, W, expert_ids, topk_weights):
+        y, r = moe_forward(x.detach(), W.detach(), expert_ids, topk_weights.detach())
+        ctx.save_for_backward(x.detach(), W.detach())
+        ctx.routing = r
+        ctx.k = expert_ids.shape[1]
+        ctx.w_dtype = topk_weights.dtype
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        x, W = ctx.saved_tensors
+        dx, dW, dtopk = moe_backward(dy, x, W, ctx.routing, ctx.k)
+        return dx.to(x.dtype), dW.to(W.dtype), None, dtopk.to(ctx.w_dtype)
+
+
+def moe(x: torch.Tensor, W: torch.Tensor, expert_ids: torch.Tensor,
+        topk_weights: torch.Tensor) -> torch.Tensor:
+    """Fused MoE layer y[t] = sum_j w[t,j] x[t] W_{ids[t,j]}^T, differentiable to
+    x, W and topk_weights ("grouped-gemm-moe", §Usage)."""
+    return _MoEFunction.apply(x, W, expert_ids, topk_weights)
+
+
+def grouped_gemm(a: torch.Tensor, W: torch.Tensor, group_sizes: torch.Tensor | None = None,
+                 end_offs: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                 out: torch.Tensor | None = None) -> torch.Tensor:
+    """Bare grouped GEMM on pre-grouped rows: out[r] = a[r] W_e^T for the
+    group e holding row r.  Give either group sizes or int32 end offsets."""
+    lib = L.load()
+    code = _dtype_code(a)
+    rows, K = a.shape
+    E, N, _ = W.shape
+    if (group_sizes is None) == (end_offs is None):
+        raise ValueError("give exactly one of group_sizes and end_offs")
+    layout = L.MGG_LAYOUT_CONTIGUOUS_SIZES if group_sizes is not None else L.MGG_LAYOUT_CONTIGUOUS
+    offs = (group_sizes if group_sizes is not None else end_offs)
+    offs = offs.to(device=a.device, dtype=torch.int32).contiguous()
+    dev = a.device
+    C = out if out is not None else torch.empty(rows, N, dtype=torch.float32, device=dev)
+    st = status if status is not None else new_status(dev)
+    nbytes = lib.mgg_workspace_bytes(L.MGG_OP_GROUPED_GEMM, 0, 0, E, N, K, code)
+    ws = _workspace(nbytes, dev)
+    L.check(lib.mgg_grouped_gemm(_ptr(a), _ptr(W), _ptr(C), code, layout, _ptr(offs), rows, E, N, K,
+                                 _ptr(st), _ptr(ws), ws.numel(), _stream()), "mgg_grouped_gemm")
+    return C
+
+
+def grouped_gemm_masked(x: torch.Tensor, W: torch.Tensor, masked_m: torch.Tensor,
+                        status: torch.Tensor | None = None,
+                        out: torch.Tensor | None = None) -> torch.Tensor:
+    """Masked decode layout: out[e, i] = x[e, i] W_e^T for i < masked_m[e];
+    other rows of ``out`` are left as they were."""
+    lib = L.load()
+    code = _dtype_code(x)
+    E, M_max, K = x.shape
+    _, N, _ = W.shape
+    dev = x.device
+    mm = masked_m.to(device=dev, dtype=torch.int32).contiguous()
+    y = out if out is not None else torch.zeros(E, M_max, N, dtype=torch.float32, device=dev)
+    st = status if status is not None else new_status(dev)
+    L.check(lib.mgg_grouped_gemm(_ptr(x), _ptr(W), _ptr(y), code, L.MGG_LAYOUT_MASKED, _ptr(mm),
+                                 M_max, E, N, K, _ptr(st), None, 0, _stream()),
+            "mgg_grouped_gemm(masked)")
+    return y
+
+
+def debug_tile_schedule(routing: RoutingBuffers, E: int, N: int, max_tiles: int,
+                        dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """The (e, mb, nb, row0, rows) the GEMM kernel decodes for each tile index;
+    rows past the device tile count stay -1."""
+    lib = L.load()
+    out = torch.full((max(max_tiles, 1), 5), -1, dtype=torch.int32, device=routing.counts.device)
+    code = L.MGG_BF16 if dtype == torch.bfloat16 else L.MGG_F32
+    rs = routing.struct()
+    L.check(lib.mgg_debug_tile_schedule(ctypes.byref(rs), E, N, code, max_tiles, _ptr(out), _stream()),
+            "mgg_debug_tile_schedule")
+    return out[:max_tiles]
