@@ -269,14 +269,25 @@ def run_ours(args, ws, rank, local):
 
 
 def load_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it is current."""
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum of
+    one ncu capture, profiles/traffic.json), or None once the kernel's source
+    has changed since the capture."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     ent = d.get(kernel)
-    return ent.get("bytes_per_launch") if isinstance(ent, dict) and ent.get("current") else None
+    if not isinstance(ent, dict):
+        return None
+    src = os.path.join(ROOT, "variable_size_expert_gb300", "csrc", ent.get("source", ""))
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != ent.get("sha256_16"):
+            return None
+    return ent.get("bytes_per_launch")
 
 
 def run_e2e(args, p, dev, lib, mgg, L, flops_step):
