@@ -359,13 +359,15 @@ def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
         t_k.append(ev.ms(0))
     fl = 2.0 * T * k * K * N
     counts = r.counts.cpu().numpy()
-    tiles = int(sum(-(-int(m) // 128) for m in counts)) * (-(-N // 256))
+    bm, bn, _ = mgg.tile_config(L.MGG_OP_FORWARD)
+    tiles = int(sum(-(-int(m) // bm) for m in counts)) * (-(-N // bn))
     res["fwd_skew"] = {
         "workload": "fused forward, Zipf(1.2) routing: T=4096, K=2048, N=1536, E=64, k=8; seed 0",
         "ms": round(statistics.mean(t_all), 4), "gemm_ms": round(statistics.mean(t_k), 4),
         "tflops": round(fl / (statistics.mean(t_all) * 1e-3) / 1e12, 1),
         "gemm_tflops": round(fl / (statistics.mean(t_k) * 1e-3) / 1e12, 1),
-        "useful_row_fraction_bm128": round(float(counts.sum()) / (128 * sum(-(-int(m) // 128) for m in counts)), 4),
+        "tile": [bm, bn],
+        "useful_row_fraction": round(float(counts.sum()) / (bm * sum(-(-int(m) // bm) for m in counts)), 4),
         "tiles": tiles, "count_min": int(counts.min()), "count_max": int(counts.max())}
     del args_, y, r
     # masked decode under CUDA-graph replay (inputs 3.8 GB >> L2)

@@ -51,7 +51,7 @@ def test_tile_config_and_workspace(lib):
     bm, bn, bk = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     assert lib.mgg_tile_config(L.MGG_OP_FORWARD, L.MGG_BF16, ctypes.byref(bm), ctypes.byref(bn),
                                ctypes.byref(bk)) == 0
-    assert (bm.value, bn.value, bk.value) == (128, 256, 64)
+    assert (bm.value, bn.value, bk.value) == (256, 256, 64)   # CTA-pair tile
     assert lib.mgg_tile_config(L.MGG_OP_FORWARD, 7, ctypes.byref(bm), ctypes.byref(bn),
                                ctypes.byref(bk)) == L.MGG_ERR_DTYPE
     # route scratch: one int per (chunk of 256 assignments, expert), 256-byte rounded

@@ -11,7 +11,13 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _check_routing(r, ids, w, E, N, BM=128, BN=256):
+def _tile():
+    bm, bn, _ = mgg.tile_config(mgg._lib.MGG_OP_FORWARD)
+    return bm, bn
+
+
+def _check_routing(r, ids, w, E, N):
+    BM, BN = _tile()
     ref = O.route(ids, w, E)
     assert np.array_equal(r.counts.cpu().numpy(), ref.counts)
     assert np.array_equal(r.end_offs.cpu().numpy(), ref.end_offs)
@@ -61,7 +67,8 @@ def test_tile_schedule_bitexact(T, k, E, N, routing, seed):
     ids, w = p["expert_ids"], p["topk_weights"]
     r = mgg.route(ids.to(DEV), w.to(DEV), E, N)
     ref = O.route(ids.numpy(), w.numpy(), E)
-    sched = O.tile_schedule(ref.counts, N, 128, 256)
+    BM, BN = _tile()
+    sched = O.tile_schedule(ref.counts, N, BM, BN)
     total = len(sched["tiles"])
     got = mgg.debug_tile_schedule(r, E, N, total + 7).cpu().numpy()
     assert np.array_equal(got[:total], sched["tiles"])

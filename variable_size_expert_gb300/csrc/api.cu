@@ -82,11 +82,21 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
+// Development switch: MGG_SINGLE_CTA=1 selects the single-CTA tensor-core
+// kernels instead of the CTA-pair ones.
+bool single_cta() {
+  static const bool v = [] {
+    const char* s = getenv("MGG_SINGLE_CTA");
+    return s && s[0] == '1';
+  }();
+  return v;
+}
+
 // Forward-path tile shape for a dtype.
 void rows_tile(mgg_dtype dt, int* BM, int* BN) {
   if (dt == MGG_BF16) {
-    *BM = kRowsBM;
-    *BN = kRowsBN;
+    *BM = single_cta() ? kRowsBM : kPairBM;
+    *BN = single_cta() ? kRowsBN : kPairBN;
   } else {
     *BM = kSimtBM;
     *BN = kSimtBN;
@@ -101,6 +111,14 @@ bool tmap_weights(CUtensorMap* m, const void* W, int E, int N, int K, int box_in
   const uint64_t strides[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2};
   const uint32_t box[3] = {static_cast<uint32_t>(box_inner), static_cast<uint32_t>(box_rows), 1};
   return encode_tmap(m, W, 3, dims, strides, box);
+}
+
+// bf16 rows [rows][cols] as a 2-D tensor map, box {64 columns, box_rows rows}.
+bool tmap_rows(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(cols) * 2};
+  const uint32_t box[2] = {64, static_cast<uint32_t>(box_rows)};
+  return encode_tmap(m, base, 2, dims, strides, box);
 }
 
 struct BwdLayout {
@@ -207,13 +225,12 @@ mgg_status mgg_tile_config(mgg_op op, mgg_dtype dtype, int* BM, int* BN, int* BK
     case MGG_OP_ROUTE:
     case MGG_OP_FORWARD:
     case MGG_OP_GROUPED_GEMM:
-      *BM = bf ? kRowsBM : kSimtBM;
-      *BN = bf ? kRowsBN : kSimtBN;
+      rows_tile(dtype, BM, BN);
       *BK = bf ? kBK : 16;
       return MGG_OK;
     case MGG_OP_BACKWARD:  // the dW tiles (dX uses the forward shape over K)
-      *BM = bf ? kDwBM : kSimtBM;
-      *BN = bf ? kDwBN : kSimtBN;
+      *BM = bf ? (single_cta() ? kDwBM : kPairBM) : kSimtBM;
+      *BN = bf ? (single_cta() ? kDwBN : kPairBN) : kSimtBN;
       *BK = bf ? kDwPad : 16;
       return MGG_OK;
     case MGG_OP_MASKED:
@@ -318,6 +335,12 @@ mgg_status mgg_grouped_gemm(const void* A, const void* W, float* C, mgg_dtype dt
     return from_cuda(timed(0, st, [&] {
       return launch_rows_f32(kModeBare, false, p, static_cast<const float*>(W), K, st);
     }));
+  if (!single_cta()) {
+    CUtensorMap tm, ta;
+    if (!tmap_weights(&tm, W, E, N, K, kBK, kPairBN / 2)) return MGG_ERR_CUDA;
+    if (!tmap_rows(&ta, A, rows_or_Mmax, K, kPairBM / 2)) return MGG_ERR_CUDA;
+    return from_cuda(timed(0, st, [&] { return launch_rows_pair(kModeBare, false, ta, tm, p, st); }));
+  }
   CUtensorMap tm;
   if (!tmap_weights(&tm, W, E, N, K, kBK, kRowsBN)) return MGG_ERR_CUDA;
   return from_cuda(timed(0, st, [&] { return launch_rows_gemm(kModeBare, false, tm, p, st); }));
@@ -365,6 +388,11 @@ mgg_status mgg_moe_forward(const void* x, const void* W, const int32_t* expert_i
     return from_cuda(timed(0, st, [&] {
       return launch_rows_f32(kModeFused, false, p, static_cast<const float*>(W), K, st);
     }));
+  if (!single_cta()) {
+    CUtensorMap tm;
+    if (!tmap_weights(&tm, W, E, N, K, kBK, kPairBN / 2)) return MGG_ERR_CUDA;
+    return from_cuda(timed(0, st, [&] { return launch_rows_pair(kModeFused, false, tm, tm, p, st); }));
+  }
   CUtensorMap tm;
   if (!tmap_weights(&tm, W, E, N, K, kBK, kRowsBN)) return MGG_ERR_CUDA;
   return from_cuda(timed(0, st, [&] { return launch_rows_gemm(kModeFused, false, tm, p, st); }));
@@ -448,8 +476,10 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   p.A = dy_b;
   CUtensorMap tm_wt;
   if (!tmap_weights(&tm_wt, W, E, N, K, 64, 64)) return MGG_ERR_CUDA;
-  if (timed(0, st, [&] { return launch_rows_gemm(kModeFusedDtopk, true, tm_wt, p, st); }) !=
-      cudaSuccess)
+  if (timed(0, st, [&] {
+        return single_cta() ? launch_rows_gemm(kModeFusedDtopk, true, tm_wt, p, st)
+                            : launch_rows_pair(kModeFusedDtopk, true, tm_wt, tm_wt, p, st);
+      }) != cudaSuccess)
     return MGG_ERR_CUDA;
 
   q.dyw = dyw;
@@ -458,7 +488,9 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   const uint64_t strides[1] = {static_cast<uint64_t>(N) * 2};
   const uint32_t box[2] = {64, static_cast<uint32_t>(kDwPad)};
   if (!encode_tmap(&tm_dyw, dyw, 2, dims, strides, box)) return MGG_ERR_CUDA;
-  return from_cuda(timed(1, st, [&] { return launch_dw_gemm(tm_dyw, q, st); }));
+  return from_cuda(timed(1, st, [&] {
+    return single_cta() ? launch_dw_gemm(tm_dyw, q, st) : launch_dw_pair(tm_dyw, q, st);
+  }));
 }
 
 mgg_status mgg_debug_tile_schedule(const mgg_routing* routing, int E, int N, mgg_dtype dtype,

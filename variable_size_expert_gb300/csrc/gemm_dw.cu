@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int kb = 0; kb < t.nkb; ++kb) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
-        if (!wait_bar(empty + 8 * s, ph ^ 1, wc)) {
+        if (!__all_sync(0xffffffffu, wait_bar(empty + 8 * s, ph ^ 1, wc))) {
           ok = false;
           break;
         }
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       const int acc = tcount & 1;
       const uint32_t use = tcount >> 1;
-      if (!wait_bar(acc_full + 8 * acc, use & 1, wc)) break;
+      if (!__all_sync(0xffffffffu, wait_bar(acc_full + 8 * acc, use & 1, wc))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
 #pragma unroll 1

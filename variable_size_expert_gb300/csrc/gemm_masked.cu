@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
-        if (!wait_bar(empty + 8 * s, ph ^ 1, wc)) {
+        if (!__all_sync(0xffffffffu, wait_bar(empty + 8 * s, ph ^ 1, wc))) {
           ok = false;
           break;
         }
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (t.m == 0) continue;
       const int acc = tcount & 1;
       const uint32_t use = tcount >> 1;
-      if (!wait_bar(acc_full + 8 * acc, use & 1, wc)) break;
+      if (!__all_sync(0xffffffffu, wait_bar(acc_full + 8 * acc, use & 1, wc))) break;
       tc_fence_after();
       const int n = t.nb * BM + warp * 32 + lane;
       float* yrow = p.y + (static_cast<long long>(t.e) * p.M_max + static_cast<long long>(t.ib) * BI) * p.N + n;

@@ -1,0 +1,662 @@
+// CTA-pair (cta_group::2) versions of the tensor-core grouped GEMMs.
+//
+// Same method as gemm_rows.cu / gemm_dw.cu ("grouped-gemm-moe", §How it
+// works: gather on load, tensor-core multiply with f32 accumulate, scale and
+// scatter-combine on store; "Grouped GEMM for MoE, in depth", §Problem
+// descriptors and the tile scheduler and §The backward pass), with the tile
+// spread over the two SMs of a cluster: one 256 x 256 tile per CTA pair, each
+// CTA loading 128 rows of A and 128 rows of B and holding its 128 rows of the
+// accumulator in its own tensor memory.  The even CTA issues the MMAs
+// (M = 256, N = 256, K = 16), which read both CTAs' operand halves.  Per SM
+// this halves the weight-tile traffic into shared memory relative to a
+// 128 x 256 single-CTA tile, which is what lets the tensor cores run near
+// their rate.
+//
+// Barriers: full[s] lives in the leader and counts the leader's expect-tx
+// arrival, the TMA bytes of both CTAs and (gather modes) the peer's relay
+// arrival (see relay_stage); gathered[s] in each CTA counts that CTA's four
+// gather warps; empty[s] and acc_full[a] live in both CTAs and are
+// signalled by the leader's multicast commits; acc_empty[a] lives in the
+// leader and counts both CTAs' four epilogue warps.
+//
+// Roles per CTA (320 threads): warps 0-3 epilogue, warp 4 TMEM allocation
+// (both CTAs), MMA issue (leader) or the gather relay (peer), warp 5 TMA for
+// B (and A in bare mode), warps 6-9 gather A rows with cp.async (gather
+// modes).
+#include <algorithm>
+
+#include "internal.h"
+#include "schedule.cuh"
+
+namespace mgg {
+namespace {
+
+constexpr int PBM = kPairBM;   // rows of a pair tile (MMA M)
+constexpr int CBM = PBM / 2;   // rows per CTA
+constexpr int PBN = kPairBN;   // columns of a pair tile (MMA N)
+constexpr int CBN = PBN / 2;   // B rows per CTA
+constexpr int BK = kBK;
+constexpr int STAGES = 6;
+constexpr int LAG = 3;         // cp.async groups a gather thread keeps in flight (< STAGES)
+constexpr int A_STAGE = CBM * BK * 2;  // 16 KB
+constexpr int B_STAGE = CBN * BK * 2;  // 16 KB
+constexpr int CHUNK = 64 * BK * 2;     // one 64-wide MN chunk of 64 K rows
+constexpr int NUM_THREADS = 320;
+constexpr int TMEM_COLS = 2 * PBN;
+constexpr int NUM_BARS = 3 * STAGES + 5;
+constexpr size_t SMEM_BYTES = 1024 + static_cast<size_t>(STAGES) * (A_STAGE + B_STAGE) + 256;
+constexpr long long DRAIN_LIMIT = 200000000LL;
+
+static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
+
+struct PairSmem {
+  uint32_t sA, sB, full, empty, gathered, acc_full, acc_empty, drain;
+  uint32_t* tmem_slot;
+  volatile int* abort_flag;
+};
+
+__device__ __forceinline__ PairSmem carve(uint8_t* smem_raw) {
+  PairSmem m;
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw_addr);
+  m.sA = base;
+  m.sB = m.sA + STAGES * A_STAGE;
+  const uint32_t bar0 = m.sB + STAGES * B_STAGE;
+  m.full = bar0;
+  m.empty = bar0 + 8 * STAGES;
+  m.gathered = bar0 + 16 * STAGES;
+  m.acc_full = bar0 + 24 * STAGES;
+  m.acc_empty = m.acc_full + 16;
+  m.drain = m.acc_full + 32;
+  m.tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar0 - base) + 8 * NUM_BARS);
+  m.abort_flag = reinterpret_cast<volatile int*>(m.tmem_slot + 1);
+  return m;
+}
+
+// The peer CTA's gathered rows reach the leader through a relay: its gather
+// warps arrive on the peer's own gathered[s] (CTA scope) once their copies
+// have completed (cp.async.wait_group) and been fenced into the async proxy,
+// and one otherwise idle thread of the peer waits there and forwards a
+// single relaxed cluster-scope arrival to the leader's full[s].  The data is
+// already complete in the peer's shared memory when the relay observes the
+// local phase, so the forward carries no release fence: a release at cluster
+// scope costs a memory barrier per stage and measured 1.5x slower overall.
+// The leader's MMA thread waits on its own gathered[s] directly.
+__device__ __forceinline__ bool relay_stage(const PairSmem& m, uint32_t full_l, int it,
+                                            const WaitCtl& wc) {
+  const int s = it % STAGES;
+  if (!wait_bar(m.gathered + 8 * s, (it / STAGES) & 1, wc)) return false;
+  mbar_arrive_cluster_relaxed(full_l + 8 * s);
+  return true;
+}
+static_assert(LAG < STAGES, "gather lag must be below the ring depth");
+
+// Barrier set-up, TMEM allocation on both CTAs, cluster-wide handshake.
+__device__ __forceinline__ uint32_t pair_setup(const PairSmem& m, uint32_t full_count, int warp) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(m.full + 8 * s, full_count);
+      mbar_init(m.empty + 8 * s, 1);
+      mbar_init(m.gathered + 8 * s, 4);  // one arrival per gather warp of this CTA
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(m.acc_full + 8 * a, 1);
+      mbar_init(m.acc_empty + 8 * a, 2 * 4);  // one arrival per epilogue warp
+    }
+    mbar_init(m.drain, 1);
+    *m.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc_cg2(smem_u32(m.tmem_slot), TMEM_COLS);
+    tmem_relinquish_cg2();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote arrival
+  tc_fence_after();
+  return *m.tmem_slot;
+}
+
+__device__ __forceinline__ void pair_teardown(uint32_t tmem_base, int warp) {
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the leader's MMAs into this CTA's TMEM are done
+  if (warp == 4) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_cg2(tmem_base, TMEM_COLS);
+  }
+}
+
+// ====================================================================== rows
+template <int MODE, bool B_MN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    rows_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                     const __grid_constant__ CUtensorMap tmap_b, const RowsParams p) {
+  constexpr bool GATHER = MODE != kModeBare;
+  extern __shared__ uint8_t smem_raw[];
+  const PairSmem m = carve(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  if (warp == 5 && lane == 0) {
+    if (!GATHER) tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  const uint32_t tmem_base = pair_setup(m, GATHER ? 2 : 1, warp);
+  const uint32_t full_l = mapa_shared(m.full, 0);           // leader's full[0]
+  const uint32_t acc_empty_l = mapa_shared(m.acc_empty, 0);  // leader's acc_empty[0]
+
+  const WaitCtl wc{m.abort_flag, p.dev_status, p.wait_limit};
+  const int total = __ldg(p.tile_start + p.E);
+  const int nkb = cdiv(p.Kc, BK);
+
+  if (warp >= 6) {
+    // ------------------------------------------------ A gather (128 threads per CTA)
+    if (GATHER) {
+      const int q = threadIdx.x - 192;
+      const int c = q & 7;
+      const int rr = q >> 3;  // this CTA's rows rr, rr+16, ..., rr+112
+      const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(p.A);
+      int it = 0;
+      bool ok = true;
+      for (int tau = pair; ok && tau < total; tau += npairs) {
+        const Tile t = decode_tile(tau, p.tile_start, p.start, p.E, PBM);
+        const __nv_bfloat16* src[8];
+        bool valid[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = static_cast<int>(rank) * CBM + rr + 16 * i;
+          valid[i] = r < t.rows;
+          const long long tok = valid[i] ? __ldg(p.row_token + t.row0 + r) : 0;
+          src[i] = A + tok * p.lda + c * 8;
+        }
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!__all_sync(0xffffffffu, wait_bar_cl(m.empty + 8 * s, ph ^ 1, wc))) {
+            ok = false;
+            break;
+          }
+          const bool kin = kb * BK + c * 8 < p.Kc;
+          const uint32_t dst = m.sA + s * A_STAGE;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const bool go = valid[i] && kin;
+            cp_async_16(dst + sw128_offset(rr + 16 * i, c),
+                        go ? static_cast<const void*>(src[i] + kb * BK) : p.A, go ? 16u : 0u);
+          }
+          cp_async_commit();
+          if (it >= LAG) {
+            cp_async_wait<LAG>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(m.gathered + 8 * ((it - LAG) % STAGES));
+          }
+          ++it;
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0)
+        for (int j = std::max(0, it - LAG); j < it; ++j) mbar_arrive(m.gathered + 8 * (j % STAGES));
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------ TMA: B half (+ A half in bare mode)
+    if (lane == 0) {
+      constexpr uint32_t TX = 2 * (B_STAGE + (GATHER ? 0 : A_STAGE));  // both CTAs
+      int it = 0;
+      bool ok = true;
+      for (int tau = pair; ok && tau < total; tau += npairs) {
+        const Tile t = decode_tile(tau, p.tile_start, p.start, p.E, PBM);
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!wait_bar_cl(m.empty + 8 * s, ph ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_l + 8 * s;
+          if (leader) mbar_arrive_expect_tx(m.full + 8 * s, TX);
+          if (!GATHER)
+            tma_load_2d_cg2(m.sA + s * A_STAGE, &tmap_a, fb, kb * BK,
+                            t.row0 + static_cast<int>(rank) * CBM);
+          const uint32_t dB = m.sB + s * B_STAGE;
+          const int n0 = t.nb * PBN + static_cast<int>(rank) * CBN;
+          if (!B_MN) {
+            tma_load_3d_cg2(dB, &tmap_b, fb, kb * BK, n0, t.e);
+          } else {
+#pragma unroll
+            for (int j = 0; j < CBN / 64; ++j)
+              tma_load_3d_cg2(dB + j * CHUNK, &tmap_b, fb, n0 + 64 * j, kb * BK, t.e);
+          }
+          ++it;
+        }
+      }
+      if (leader)
+        for (int j = std::max(0, it - STAGES); j < it; ++j)
+          wait_bar_drain(m.full + 8 * (j % STAGES), (j / STAGES) & 1, DRAIN_LIMIT);
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------ MMA issue (leader) / relay (peer)
+    if (!leader && GATHER && lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int tau = pair; ok && tau < total; tau += npairs)
+        for (int kb = 0; kb < nkb; ++kb, ++it)
+          if (!relay_stage(m, full_l, it, wc)) {
+            ok = false;
+            break;
+          }
+    }
+    if (leader && lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(PBM, PBN, false, B_MN);
+      int it = 0, tcount = 0;
+      bool ok = true;
+      for (int tau = pair; ok && tau < total; tau += npairs) {
+        const int acc = tcount & 1;
+        const uint32_t use = tcount >> 1;
+        if (!wait_bar_cl(m.acc_empty + 8 * acc, (use & 1) ^ 1, wc)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * PBN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!wait_bar_cl(m.full + 8 * s, ph, wc) ||
+              (GATHER && !wait_bar(m.gathered + 8 * s, ph, wc))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = m.sA + s * A_STAGE;
+          const uint32_t b0 = m.sB + s * B_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t adesc = sw128_desc(a0 + kk * 32, 16, 1024);
+            const uint64_t bdesc = B_MN ? sw128_desc(b0 + kk * 16 * 128, CHUNK, 1024)
+                                        : sw128_desc(b0 + kk * 32, 16, 1024);
+            tc_mma_bf16_cg2(d, adesc, bdesc, IDESC, (kb | kk) != 0);
+          }
+          tc_commit_cg2_mc(m.empty + 8 * s, 0x3);
+          ++it;
+        }
+        if (!ok) break;
+        tc_commit_cg2_mc(m.acc_full + 8 * acc, 0x3);
+        ++tcount;
+      }
+      tc_commit_cg2(m.drain);
+      wait_bar_drain(m.drain, 0, DRAIN_LIMIT);
+    }
+  } else {
+    // ------------------------------------------------ epilogue (128 threads per CTA)
+    const int r = static_cast<int>(rank) * CBM + warp * 32 + lane;  // row within the pair tile
+    int tcount = 0;
+    for (int tau = pair; tau < total; tau += npairs) {
+      const Tile t = decode_tile(tau, p.tile_start, p.start, p.E, PBM);
+      const int acc = tcount & 1;
+      const uint32_t use = tcount >> 1;
+      if (!__all_sync(0xffffffffu, wait_bar_cl(m.acc_full + 8 * acc, use & 1, wc))) break;
+      tc_fence_after();
+      const bool valid = r < t.rows;
+      const int row = t.row0 + r;
+      long long orow = row;
+      float wr = 1.f;
+      if (MODE != kModeBare && valid) {
+        orow = __ldg(p.row_token + row);
+        wr = __ldg(p.row_weight + row);
+      }
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * PBN;
+      const int n0 = t.nb * PBN;
+      float dot = 0.f;
+#pragma unroll 1
+      for (int cc = 0; cc < PBN / 32; ++cc) {
+        const int col = n0 + cc * 32;
+        if (col >= p.Nout) break;  // uniform over the pair
+        float v[32];
+        tmem_ld32(taddr + cc * 32, v);
+        tmem_ld_wait();
+        if (valid) {
+          float* o = p.out + orow * p.ldo + col;
+          if (MODE == kModeBare) {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              if (col + 4 * q4 < p.Nout)
+                *reinterpret_cast<float4*>(o + 4 * q4) =
+                    make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+          } else {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              if (col + 4 * q4 < p.Nout)
+                atomicAdd(reinterpret_cast<float4*>(o + 4 * q4),
+                          make_float4(wr * v[4 * q4], wr * v[4 * q4 + 1], wr * v[4 * q4 + 2],
+                                      wr * v[4 * q4 + 3]));
+            if (MODE == kModeFusedDtopk) {
+              const __nv_bfloat16* xr =
+                  static_cast<const __nv_bfloat16*>(p.xdot) + orow * p.ldx + col;
+#pragma unroll
+              for (int q8 = 0; q8 < 4; ++q8) {
+                if (col + 8 * q8 < p.Nout) {
+                  const uint4 u = __ldg(reinterpret_cast<const uint4*>(xr + 8 * q8));
+                  const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                  for (int h = 0; h < 4; ++h) {
+                    const float lo = __uint_as_float(wds[h] << 16);
+                    const float hi = __uint_as_float(wds[h] & 0xFFFF0000u);
+                    dot = fmaf(lo, v[8 * q8 + 2 * h], dot);
+                    dot = fmaf(hi, v[8 * q8 + 2 * h + 1], dot);
+                  }
+                }
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
+      if (MODE == kModeFusedDtopk && valid) atomicAdd(p.dtopk + __ldg(p.row_assign + row), dot);
+      ++tcount;
+    }
+  }
+
+  pair_teardown(tmem_base, warp);
+}
+
+// ====================================================================== dW
+struct DwTile {
+  int e, kbo, nb, m, nkb;
+};
+
+__device__ __forceinline__ DwTile decode_dw(int tau, int tiles_k, int tiles_n,
+                                            const int32_t* __restrict__ counts) {
+  DwTile t;
+  const int per = tiles_k * tiles_n;
+  t.e = tau / per;
+  const int local = tau - t.e * per;
+  t.nb = local / tiles_k;
+  t.kbo = local - t.nb * tiles_k;
+  t.m = __ldg(counts + t.e);
+  t.nkb = cdiv(t.m, BK);
+  return t;
+}
+
+// dW_e tile D[k, n], 256 k-columns (128 per CTA) x 256 n-columns, contraction
+// over the expert's rows in steps of 64.  A = x rows gathered through
+// row_token (MN-major, this CTA's 128 k-columns as two 64-wide chunks); B =
+// the scaled, expert-sorted dY operand (MN-major, this CTA's 128 n-columns)
+// by TMA.  Rows past m_e are zero-filled on the x side and zero-padded on
+// the dY side.  Tiles of experts with no rows write zeros.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    dw_pair_kernel(const __grid_constant__ CUtensorMap tmap_dyw, const DwParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const PairSmem m = carve(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  if (warp == 5 && lane == 0) tma_prefetch_desc(&tmap_dyw);
+  const uint32_t tmem_base = pair_setup(m, 2, warp);
+  const uint32_t full_l = mapa_shared(m.full, 0);
+  const uint32_t acc_empty_l = mapa_shared(m.acc_empty, 0);
+
+  const WaitCtl wc{m.abort_flag, p.dev_status, p.wait_limit};
+  const int tiles_k = cdiv(p.K, PBM);
+  const int tiles_n = cdiv(p.N, PBN);
+  const int total = p.E * tiles_k * tiles_n;
+
+  if (warp >= 6) {
+    // ------------------------------------------------ x gather (128 threads per CTA)
+    const int q = threadIdx.x - 192;
+    const int c = q & 7;
+    const int rr = q >> 3;  // rows rr + 16 i (i = 0..3) of the stage, both k chunks
+    const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(p.x);
+    int it = 0;
+    bool ok = true;
+    for (int tau = pair; ok && tau < total; tau += npairs) {
+      const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts);
+      const int s0 = __ldg(p.start + t.e);
+      const int k0 = t.kbo * PBM + static_cast<int>(rank) * CBM;
+      for (int kb = 0; kb < t.nkb; ++kb) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        long long tok[4];
+        bool rv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int lr = kb * BK + rr + 16 * i;
+          rv[i] = lr < t.m;
+          tok[i] = rv[i] ? __ldg(p.row_token + s0 + lr) : 0;
+        }
+        if (!__all_sync(0xffffffffu, wait_bar_cl(m.empty + 8 * s, ph ^ 1, wc))) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = m.sA + s * A_STAGE;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+          for (int j = 0; j < CBM / 64; ++j) {
+            const int kcol = k0 + 64 * j + c * 8;
+            const bool go = rv[i] && kcol < p.K;
+            cp_async_16(dst + j * CHUNK + sw128_offset(rr + 16 * i, c),
+                        go ? static_cast<const void*>(X + tok[i] * p.K + kcol) : p.x,
+                        go ? 16u : 0u);
+          }
+        }
+        cp_async_commit();
+        if (it >= LAG) {
+          cp_async_wait<LAG>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(m.gathered + 8 * ((it - LAG) % STAGES));
+        }
+        ++it;
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0)
+      for (int j = std::max(0, it - LAG); j < it; ++j) mbar_arrive(m.gathered + 8 * (j % STAGES));
+  } else if (warp == 5) {
+    // ------------------------------------------------ scaled dY by TMA
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int tau = pair; ok && tau < total; tau += npairs) {
+        const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts);
+        const int ps = __ldg(p.pstart + t.e);
+        const int n0 = t.nb * PBN + static_cast<int>(rank) * CBN;
+        for (int kb = 0; kb < t.nkb; ++kb) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!wait_bar_cl(m.empty + 8 * s, ph ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(m.full + 8 * s, 2 * B_STAGE);
+          const uint32_t dB = m.sB + s * B_STAGE;
+#pragma unroll
+          for (int j = 0; j < CBN / 64; ++j)
+            tma_load_2d_cg2(dB + j * CHUNK, &tmap_dyw, full_l + 8 * s, n0 + 64 * j, ps + kb * BK);
+          ++it;
+        }
+      }
+      if (leader)
+        for (int j = std::max(0, it - STAGES); j < it; ++j)
+          wait_bar_drain(m.full + 8 * (j % STAGES), (j / STAGES) & 1, DRAIN_LIMIT);
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------ MMA issue (leader) / relay (peer)
+    if (!leader && lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int tau = pair; ok && tau < total; tau += npairs) {
+        const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts);
+        for (int kb = 0; kb < t.nkb; ++kb, ++it)
+          if (!relay_stage(m, full_l, it, wc)) {
+            ok = false;
+            break;
+          }
+      }
+    }
+    if (leader && lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(PBM, PBN, true, true);
+      int it = 0, tcount = 0;
+      bool ok = true;
+      for (int tau = pair; ok && tau < total; tau += npairs) {
+        const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts);
+        if (t.nkb == 0) continue;
+        const int acc = tcount & 1;
+        const uint32_t use = tcount >> 1;
+        if (!wait_bar_cl(m.acc_empty + 8 * acc, (use & 1) ^ 1, wc)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * PBN;
+        for (int kb = 0; kb < t.nkb; ++kb) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!wait_bar_cl(m.full + 8 * s, ph, wc) || !wait_bar(m.gathered + 8 * s, ph, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = m.sA + s * A_STAGE;
+          const uint32_t b0 = m.sB + s * B_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_bf16_cg2(d, sw128_desc(a0 + kk * 16 * 128, CHUNK, 1024),
+                            sw128_desc(b0 + kk * 16 * 128, CHUNK, 1024), IDESC, (kb | kk) != 0);
+          tc_commit_cg2_mc(m.empty + 8 * s, 0x3);
+          ++it;
+        }
+        if (!ok) break;
+        tc_commit_cg2_mc(m.acc_full + 8 * acc, 0x3);
+        ++tcount;
+      }
+      tc_commit_cg2(m.drain);
+      wait_bar_drain(m.drain, 0, DRAIN_LIMIT);
+    }
+  } else {
+    // ------------------------------------------------ epilogue (128 threads per CTA)
+    int tcount = 0;
+    for (int tau = pair; tau < total; tau += npairs) {
+      const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts);
+      const int kcol = t.kbo * PBM + static_cast<int>(rank) * CBM + warp * 32 + lane;
+      float* out = p.dW + static_cast<size_t>(t.e) * p.N * p.K + kcol;
+      const int n0 = t.nb * PBN;
+      if (t.nkb == 0) {
+        // expert with no rows: its gradient is exactly zero, and is written
+        if (kcol < p.K)
+          for (int n = n0; n < min(n0 + PBN, p.N); ++n) out[static_cast<size_t>(n) * p.K] = 0.f;
+        continue;
+      }
+      const int acc = tcount & 1;
+      const uint32_t use = tcount >> 1;
+      if (!__all_sync(0xffffffffu, wait_bar_cl(m.acc_full + 8 * acc, use & 1, wc))) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * PBN;
+#pragma unroll 1
+      for (int cc = 0; cc < PBN / 32; ++cc) {
+        const int n = n0 + cc * 32;
+        if (n >= p.N) break;
+        float v[32];
+        tmem_ld32(taddr + cc * 32, v);
+        tmem_ld_wait();
+        if (kcol < p.K) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (n + i < p.N) out[static_cast<size_t>(n + i) * p.K] = v[i];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
+      ++tcount;
+    }
+  }
+
+  pair_teardown(tmem_base, warp);
+}
+
+// Largest grid of co-resident pairs (a persistent kernel must not have
+// clusters waiting for others to finish).
+template <typename K>
+int pair_grid(K kern) {
+  static int cache[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && cache[dev]) return cache[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms() & ~1, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1)
+    clusters = num_sms() / 2;
+  const int g = 2 * std::min(clusters, num_sms() / 2);
+  if (dev < 64) cache[dev] = g;
+  return g;
+}
+
+template <typename K>
+cudaError_t prepare(K kern, bool* done) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && done[dev]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  if (dev < 64) done[dev] = true;
+  return cudaSuccess;
+}
+
+template <int MODE, bool B_MN>
+cudaError_t launch_rows_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, const RowsParams& p,
+                               cudaStream_t st) {
+  auto kern = rows_pair_kernel<MODE, B_MN>;
+  static bool done[64] = {};
+  cudaError_t e = prepare(kern, done);
+  if (e != cudaSuccess) return e;
+  kern<<<pair_grid(kern), NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_a,
+                             const CUtensorMap& tmap_b, const RowsParams& p, cudaStream_t st) {
+  if (!b_mn_major) {
+    if (mode == kModeBare) return launch_rows_pair_t<kModeBare, false>(tmap_a, tmap_b, p, st);
+    if (mode == kModeFused) return launch_rows_pair_t<kModeFused, false>(tmap_a, tmap_b, p, st);
+  } else {
+    if (mode == kModeFusedDtopk)
+      return launch_rows_pair_t<kModeFusedDtopk, true>(tmap_a, tmap_b, p, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_dw_pair(const CUtensorMap& tmap_dyw, const DwParams& p, cudaStream_t st) {
+  static bool done[64] = {};
+  cudaError_t e = prepare(dw_pair_kernel, done);
+  if (e != cudaSuccess) return e;
+  dw_pair_kernel<<<pair_grid(dw_pair_kernel), NUM_THREADS, SMEM_BYTES, st>>>(tmap_dyw, p);
+  return cudaGetLastError();
+}
+
+}  // namespace mgg

@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
-        if (!wait_bar(empty + 8 * s, ph ^ 1, wc)) {
+        if (!__all_sync(0xffffffffu, wait_bar(empty + 8 * s, ph ^ 1, wc))) {
           ok = false;
           break;
         }
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Tile t = decode_tile(tau, p.tile_start, p.start, p.E, BM);
       const int acc = tcount & 1;
       const uint32_t use = tcount >> 1;
-      if (!wait_bar(acc_full + 8 * acc, use & 1, wc)) break;
+      if (!__all_sync(0xffffffffu, wait_bar(acc_full + 8 * acc, use & 1, wc))) break;
       tc_fence_after();
       const bool valid = r < t.rows;
       const int row = t.row0 + r;

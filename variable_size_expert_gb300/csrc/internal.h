@@ -10,6 +10,8 @@
 namespace mgg {
 
 // Tile shapes of the tensor-core kernels.
+constexpr int kPairBM = 256;   // CTA-pair tile rows (MMA M, 128 per CTA)
+constexpr int kPairBN = 256;   // CTA-pair tile columns (MMA N, B split 128 per CTA)
 constexpr int kRowsBM = 128;   // rows (assignments) per tile: MMA M
 constexpr int kRowsBN = 256;   // output columns per tile: MMA N
 constexpr int kBK = 64;        // contraction step: one 128-byte swizzle row of bf16
@@ -103,6 +105,10 @@ cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* star
 // gemm_rows.cu (tcgen05)
 cudaError_t launch_rows_gemm(int mode, bool b_mn_major, const CUtensorMap& tmap_b,
                              const RowsParams& p, cudaStream_t st);
+// gemm_pair.cu (tcgen05, cta_group::2)
+cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_a,
+                             const CUtensorMap& tmap_b, const RowsParams& p, cudaStream_t st);
+cudaError_t launch_dw_pair(const CUtensorMap& tmap_dyw, const DwParams& p, cudaStream_t st);
 // gemm_dw.cu (tcgen05)
 cudaError_t launch_dw_gemm(const CUtensorMap& tmap_dyw, const DwParams& p, cudaStream_t st);
 // gemm_masked.cu (tcgen05)
