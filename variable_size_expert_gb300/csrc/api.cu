@@ -470,8 +470,9 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
 
   void* dy_b = at<void>(ws, L.off_dy_b);
   void* dyw = at<void>(ws, L.off_dyw);
-  if (launch_bwd_prep(dy, T, N, routing->counts, routing->start, pstart, routing->row_token,
-                      routing->row_weight, E, L.S_pad_max, dy_b, dyw, st) != cudaSuccess)
+  if (launch_bwd_prep(dy, N, k, routing->counts, routing->start, pstart, routing->row_token,
+                      routing->row_assign, routing->row_weight, E, L.S_pad_max, dy_b, dyw,
+                      st) != cudaSuccess)
     return MGG_ERR_CUDA;
   p.A = dy_b;
   CUtensorMap tm_wt;

@@ -95,10 +95,10 @@ cudaError_t launch_offsets_scan(const int32_t* offs, bool is_sizes, int E, int r
                                 int32_t* dev_status, cudaStream_t st);
 cudaError_t launch_bwd_scan(const int32_t* counts, int E, int BM, int tiles_n, int pad,
                             int32_t* tile_start_dx, int32_t* pstart, cudaStream_t st);
-cudaError_t launch_bwd_prep(const float* dy, int T, int N, const int32_t* counts,
+cudaError_t launch_bwd_prep(const float* dy, int N, int k, const int32_t* counts,
                             const int32_t* start, const int32_t* pstart, const int32_t* row_token,
-                            const float* row_weight, int E, int S_pad_max, void* dy_b, void* dyw,
-                            cudaStream_t st);
+                            const int32_t* row_assign, const float* row_weight, int E,
+                            int S_pad_max, void* dy_b, void* dyw, cudaStream_t st);
 cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* start, int E, int BM,
                                   int max_tiles, int32_t* out, cudaStream_t st);
 

@@ -196,32 +196,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
          (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
-// dy_b = bf16(dy), 8 elements per thread (N % 8 == 0).
-__global__ void cast_bf16_kernel(const float* __restrict__ src, uint4* __restrict__ dst,
-                                 size_t n8) {
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(src)[2 * i];
-    const float4 b = reinterpret_cast<const float4*>(src)[2 * i + 1];
-    uint4 o;
-    o.x = pack_bf16x2(a.x, a.y);
-    o.y = pack_bf16x2(a.z, a.w);
-    o.z = pack_bf16x2(b.x, b.y);
-    o.w = pack_bf16x2(b.z, b.w);
-    dst[i] = o;
-  }
-}
-
-// Scaled, expert-sorted dY for dW: padded row p of expert e holds
-// bf16(fl32(w_r * dy[token_r])) for its sorted row r, or zeros in the
-// padding.  One block per padded row.
-__global__ void dyw_prep_kernel(const float* __restrict__ dy, int N,
+// Backward operands in one pass over dy, one block per padded row p of the
+// scaled, expert-sorted dY operand of dW:
+//   dyw[p]   = bf16(fl32(w_r * dy[token_r]))  for the sorted row r held in p,
+//              zeros in the padding rows of each expert's segment;
+//   dy_b[t]  = bf16(dy[t]), written by the row whose assignment is token t's
+//              first (a = t*k), so every token row is written exactly once.
+// N % 8 == 0; 8 elements per thread step.
+__global__ void bwd_prep_kernel(const float* __restrict__ dy, int N, int k,
                                 const int32_t* __restrict__ counts,
                                 const int32_t* __restrict__ start,
                                 const int32_t* __restrict__ pstart,
                                 const int32_t* __restrict__ row_token,
+                                const int32_t* __restrict__ row_assign,
                                 const float* __restrict__ row_weight, int E,
-                                uint4* __restrict__ dyw) {
+                                uint4* __restrict__ dyw, uint4* __restrict__ dy_b) {
   const int p = blockIdx.x;
   if (p >= __ldg(pstart + E)) return;
   int lo = 0, hi = E + 1;  // expert whose padded segment holds p
@@ -242,7 +231,10 @@ __global__ void dyw_prep_kernel(const float* __restrict__ dy, int N,
   }
   const int r = __ldg(start + e) + local;
   const float wr = __ldg(row_weight + r);
-  const float4* src = reinterpret_cast<const float4*>(dy + static_cast<size_t>(__ldg(row_token + r)) * N);
+  const int tok = __ldg(row_token + r);
+  const bool first = __ldg(row_assign + r) % k == 0;
+  const float4* src = reinterpret_cast<const float4*>(dy + static_cast<size_t>(tok) * N);
+  uint4* outb = dy_b + static_cast<size_t>(tok) * n8;
   for (int i = threadIdx.x; i < n8; i += blockDim.x) {
     const float4 a = src[2 * i];
     const float4 b = src[2 * i + 1];
@@ -252,6 +244,14 @@ __global__ void dyw_prep_kernel(const float* __restrict__ dy, int N,
     o.z = pack_bf16x2(__fmul_rn(wr, b.x), __fmul_rn(wr, b.y));
     o.w = pack_bf16x2(__fmul_rn(wr, b.z), __fmul_rn(wr, b.w));
     out[i] = o;
+    if (first) {
+      uint4 q;
+      q.x = pack_bf16x2(a.x, a.y);
+      q.y = pack_bf16x2(a.z, a.w);
+      q.z = pack_bf16x2(b.x, b.y);
+      q.w = pack_bf16x2(b.z, b.w);
+      outb[i] = q;
+    }
   }
 }
 
@@ -308,16 +308,14 @@ cudaError_t launch_bwd_scan(const int32_t* counts, int E, int BM, int tiles_n, i
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_prep(const float* dy, int T, int N, const int32_t* counts,
+cudaError_t launch_bwd_prep(const float* dy, int N, int k, const int32_t* counts,
                             const int32_t* start, const int32_t* pstart, const int32_t* row_token,
-                            const float* row_weight, int E, int S_pad_max, void* dy_b, void* dyw,
-                            cudaStream_t st) {
-  const size_t n8 = static_cast<size_t>(T) * N / 8;
-  const int blocks = static_cast<int>(std::min<size_t>((n8 + 255) / 256, 65536));
-  cast_bf16_kernel<<<blocks, 256, 0, st>>>(dy, static_cast<uint4*>(dy_b), n8);
+                            const int32_t* row_assign, const float* row_weight, int E,
+                            int S_pad_max, void* dy_b, void* dyw, cudaStream_t st) {
   if (S_pad_max > 0)
-    dyw_prep_kernel<<<S_pad_max, 256, 0, st>>>(dy, N, counts, start, pstart, row_token,
-                                               row_weight, E, static_cast<uint4*>(dyw));
+    bwd_prep_kernel<<<S_pad_max, 256, 0, st>>>(dy, N, k, counts, start, pstart, row_token,
+                                               row_assign, row_weight, E,
+                                               static_cast<uint4*>(dyw), static_cast<uint4*>(dy_b));
   return cudaGetLastError();
 }
 
