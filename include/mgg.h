@@ -154,6 +154,39 @@ mgg_status mgg_route(const int32_t* expert_ids, const float* topk_weights, int T
                      size_t ws_bytes, void* stream);
 
 /*
+ * Size of the device array mgg_route_noalloc uses as scratch (1 MiB).
+ */
+#define MGG_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/*
+ * mgg_route without a caller workspace (the pages have no counterpart: this
+ * is an interface convenience).  For callers that cannot allocate device
+ * memory when they route, e.g. code inside a sealed memory arena that only
+ * hands out planned tensors, or a host path where a cudaMalloc would
+ * synchronise the device.  Arguments and results are those of mgg_route
+ * minus ws/ws_bytes; the router's per-chunk expert histogram lives instead
+ * in a 1 MiB device array (MGG_NOALLOC_SCRATCH_BYTES) that every GPU which
+ * loads the library reserves once and keeps until the process exits.
+ *   - Nothing is allocated or freed by the call (no cudaMalloc, cudaFree or
+ *     allocating library routine).
+ *   - Limit: ceil(T*k/256) * E * 4 bytes must fit in the array (for
+ *     example T*k <= 65536 with E = 1024, or T*k <= 1048576 with E = 64);
+ *     larger problems return MGG_ERR_WORKSPACE without launching.
+ *   - The first call on a device looks up that device's array address
+ *     (cudaGetSymbolAddress, with the device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last
+ *     call's contents; the router overwrites every entry it reads, so no
+ *     clearing is needed.  Calls whose work overlaps on the GPU (other
+ *     streams, or host threads issuing concurrently) race on the array:
+ *     serialise them.
+ * Errors: as mgg_route, plus MGG_ERR_WORKSPACE for problems over the limit.
+ */
+mgg_status mgg_route_noalloc(const int32_t* expert_ids, const float* topk_weights, int T, int k,
+                             int E, int N, mgg_dtype dtype, const mgg_routing* routing,
+                             int32_t* dev_status, void* stream);
+
+/*
  * Bare variable-size grouped GEMM: the fused kernel with the permutation
  * maps omitted, rows already grouped and written in order
  * ("grouped-gemm-moe", §How it works, last paragraph; §Usage).

@@ -37,12 +37,13 @@ MGG_DEV_BAD_EXPERT_ID = 0x1
 MGG_DEV_BAD_OFFSETS = 0x2
 MGG_DEV_TIMEOUT = 0x4
 MGG_MAX_EXPERTS = 1024
+MGG_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 # every exported symbol of include/mgg.h
 EXPORTS = (
     "mgg_status_string", "mgg_tile_config", "mgg_workspace_bytes", "mgg_route",
     "mgg_grouped_gemm", "mgg_moe_forward", "mgg_moe_backward", "mgg_debug_tile_schedule",
-    "mgg_set_kernel_events",
+    "mgg_set_kernel_events", "mgg_route_noalloc",
 )
 
 
@@ -73,6 +74,7 @@ _SIGS = {
     "mgg_moe_backward": (_I, [_P, _P, _P, _RP, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "mgg_debug_tile_schedule": (_I, [_RP, _I, _I, _I, _I, _P, _P]),
     "mgg_set_kernel_events": (_I, [ctypes.POINTER(_P), _I]),
+    "mgg_route_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _RP, _P, _P]),
 }
 
 _lib = None
