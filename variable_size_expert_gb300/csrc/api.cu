@@ -82,21 +82,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
-// Development switch: MGG_SINGLE_CTA=1 selects the single-CTA tensor-core
-// kernels instead of the CTA-pair ones.
-bool single_cta() {
-  static const bool v = [] {
-    const char* s = getenv("MGG_SINGLE_CTA");
-    return s && s[0] == '1';
-  }();
-  return v;
-}
-
-// Forward-path tile shape for a dtype.
+// Forward-path tile shape for a dtype (bf16: one CTA-pair tile).
 void rows_tile(mgg_dtype dt, int* BM, int* BN) {
   if (dt == MGG_BF16) {
-    *BM = single_cta() ? kRowsBM : kPairBM;
-    *BN = single_cta() ? kRowsBN : kPairBN;
+    *BM = kPairBM;
+    *BN = kPairBN;
   } else {
     *BM = kSimtBM;
     *BN = kSimtBN;
@@ -229,8 +219,8 @@ mgg_status mgg_tile_config(mgg_op op, mgg_dtype dtype, int* BM, int* BN, int* BK
       *BK = bf ? kBK : 16;
       return MGG_OK;
     case MGG_OP_BACKWARD:  // the dW tiles (dX uses the forward shape over K)
-      *BM = bf ? (single_cta() ? kDwBM : kPairBM) : kSimtBM;
-      *BN = bf ? (single_cta() ? kDwBN : kPairBN) : kSimtBN;
+      *BM = bf ? kPairBM : kSimtBM;
+      *BN = bf ? kPairBN : kSimtBN;
       *BK = bf ? kDwPad : 16;
       return MGG_OK;
     case MGG_OP_MASKED:
@@ -335,15 +325,10 @@ mgg_status mgg_grouped_gemm(const void* A, const void* W, float* C, mgg_dtype dt
     return from_cuda(timed(0, st, [&] {
       return launch_rows_f32(kModeBare, false, p, static_cast<const float*>(W), K, st);
     }));
-  if (!single_cta()) {
-    CUtensorMap tm, ta;
-    if (!tmap_weights(&tm, W, E, N, K, kBK, kPairBN / 2)) return MGG_ERR_CUDA;
-    if (!tmap_rows(&ta, A, rows_or_Mmax, K, kPairBM / 2)) return MGG_ERR_CUDA;
-    return from_cuda(timed(0, st, [&] { return launch_rows_pair(kModeBare, false, ta, tm, p, st); }));
-  }
-  CUtensorMap tm;
-  if (!tmap_weights(&tm, W, E, N, K, kBK, kRowsBN)) return MGG_ERR_CUDA;
-  return from_cuda(timed(0, st, [&] { return launch_rows_gemm(kModeBare, false, tm, p, st); }));
+  CUtensorMap tm, ta;
+  if (!tmap_weights(&tm, W, E, N, K, kBK, kPairBN / 2)) return MGG_ERR_CUDA;
+  if (!tmap_rows(&ta, A, rows_or_Mmax, K, kPairBM / 2)) return MGG_ERR_CUDA;
+  return from_cuda(timed(0, st, [&] { return launch_rows_pair(kModeBare, false, ta, tm, p, st); }));
 }
 
 mgg_status mgg_moe_forward(const void* x, const void* W, const int32_t* expert_ids,
@@ -388,14 +373,9 @@ mgg_status mgg_moe_forward(const void* x, const void* W, const int32_t* expert_i
     return from_cuda(timed(0, st, [&] {
       return launch_rows_f32(kModeFused, false, p, static_cast<const float*>(W), K, st);
     }));
-  if (!single_cta()) {
-    CUtensorMap tm;
-    if (!tmap_weights(&tm, W, E, N, K, kBK, kPairBN / 2)) return MGG_ERR_CUDA;
-    return from_cuda(timed(0, st, [&] { return launch_rows_pair(kModeFused, false, tm, tm, p, st); }));
-  }
   CUtensorMap tm;
-  if (!tmap_weights(&tm, W, E, N, K, kBK, kRowsBN)) return MGG_ERR_CUDA;
-  return from_cuda(timed(0, st, [&] { return launch_rows_gemm(kModeFused, false, tm, p, st); }));
+  if (!tmap_weights(&tm, W, E, N, K, kBK, kPairBN / 2)) return MGG_ERR_CUDA;
+  return from_cuda(timed(0, st, [&] { return launch_rows_pair(kModeFused, false, tm, tm, p, st); }));
 }
 
 mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
@@ -477,10 +457,8 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   p.A = dy_b;
   CUtensorMap tm_wt;
   if (!tmap_weights(&tm_wt, W, E, N, K, 64, 64)) return MGG_ERR_CUDA;
-  if (timed(0, st, [&] {
-        return single_cta() ? launch_rows_gemm(kModeFusedDtopk, true, tm_wt, p, st)
-                            : launch_rows_pair(kModeFusedDtopk, true, tm_wt, tm_wt, p, st);
-      }) != cudaSuccess)
+  if (timed(0, st, [&] { return launch_rows_pair(kModeFusedDtopk, true, tm_wt, tm_wt, p, st); }) !=
+      cudaSuccess)
     return MGG_ERR_CUDA;
 
   q.dyw = dyw;
@@ -489,9 +467,7 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   const uint64_t strides[1] = {static_cast<uint64_t>(N) * 2};
   const uint32_t box[2] = {64, static_cast<uint32_t>(kDwPad)};
   if (!encode_tmap(&tm_dyw, dyw, 2, dims, strides, box)) return MGG_ERR_CUDA;
-  return from_cuda(timed(1, st, [&] {
-    return single_cta() ? launch_dw_gemm(tm_dyw, q, st) : launch_dw_pair(tm_dyw, q, st);
-  }));
+  return from_cuda(timed(1, st, [&] { return launch_dw_pair(tm_dyw, q, st); }));
 }
 
 mgg_status mgg_debug_tile_schedule(const mgg_routing* routing, int E, int N, mgg_dtype dtype,

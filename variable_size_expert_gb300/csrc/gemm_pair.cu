@@ -1,16 +1,31 @@
-// CTA-pair (cta_group::2) versions of the tensor-core grouped GEMMs.
+// Tensor-core grouped GEMMs on CTA pairs (tcgen05, cta_group::2): the fused
+// MoE forward, the bare grouped GEMM, the backward dX (with d routing
+// weight) and the backward dW.
 //
-// Same method as gemm_rows.cu / gemm_dw.cu ("grouped-gemm-moe", §How it
-// works: gather on load, tensor-core multiply with f32 accumulate, scale and
-// scatter-combine on store; "Grouped GEMM for MoE, in depth", §Problem
-// descriptors and the tile scheduler and §The backward pass), with the tile
-// spread over the two SMs of a cluster: one 256 x 256 tile per CTA pair, each
-// CTA loading 128 rows of A and 128 rows of B and holding its 128 rows of the
-// accumulator in its own tensor memory.  The even CTA issues the MMAs
-// (M = 256, N = 256, K = 16), which read both CTAs' operand halves.  Per SM
-// this halves the weight-tile traffic into shared memory relative to a
-// 128 x 256 single-CTA tile, which is what lets the tensor cores run near
-// their rate.
+// Per tile of one expert ("grouped-gemm-moe", §How it works):
+//   * gather on load: activation rows are read through the row->token map
+//     straight into shared memory (the permuted [S, K] tensor is never
+//     stored);
+//   * multiply against the tile's expert weight on the tensor cores with an
+//     f32 accumulator in tensor memory;
+//   * scatter on store: each row is scaled by its routing weight and added
+//     atomically into its token's output row (top-k combine in place; the
+//     expanded [S, N] output is never stored).
+// The bare grouped GEMM is the same kernel with the maps omitted (rows in
+// order, plain stores).  dX is the forward run on bf16(dy) with each W_e read
+// transposed ("Grouped GEMM for MoE, in depth", §The backward pass); its
+// epilogue also forms d(routing weight) = <dy W_e, x> = <dy, x W_e^T>.  dW_e
+// is a per-expert A^T B over the expert's rows (same page, weight gradient).
+//
+// The grid is persistent: one cluster of two CTAs per SM pair loops over the
+// flat tile space with stride = number of pairs ("Grouped GEMM for MoE, in
+// depth", §Problem descriptors and the tile scheduler).  Each 256 x 256 tile
+// is spread over the two SMs: each CTA loads 128 rows of A and 128 rows of B
+// and holds its 128 rows of the accumulator in its own tensor memory; the
+// even CTA ("leader") issues the MMAs (M = 256, N = 256, K = 16), which read
+// both CTAs' operand halves.  Against a 128 x 256 single-CTA tile this halves
+// the weight bytes each SM pulls per FLOP, and the kernels are bound by the
+// bytes L2 can deliver to the SMs.
 //
 // Barriers: full[s] lives in the leader and counts the leader's expect-tx
 // arrival, the TMA bytes of both CTAs and (gather modes) the peer's relay

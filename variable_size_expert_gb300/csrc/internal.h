@@ -12,11 +12,7 @@ namespace mgg {
 // Tile shapes of the tensor-core kernels.
 constexpr int kPairBM = 256;   // CTA-pair tile rows (MMA M, 128 per CTA)
 constexpr int kPairBN = 256;   // CTA-pair tile columns (MMA N, B split 128 per CTA)
-constexpr int kRowsBM = 128;   // rows (assignments) per tile: MMA M
-constexpr int kRowsBN = 256;   // output columns per tile: MMA N
 constexpr int kBK = 64;        // contraction step: one 128-byte swizzle row of bf16
-constexpr int kDwBM = 128;     // dW tile: K-output rows (MMA M)
-constexpr int kDwBN = 256;     // dW tile: N-output columns (MMA N)
 constexpr int kDwPad = 64;     // expert segments of the scaled dY operand are padded to this
 constexpr int kMaskedBM = 128; // decode tile: weight rows (MMA M)
 constexpr int kMaskedBI = 64;  // decode tile: activation rows per tile (MMA N <= 64)
@@ -102,15 +98,10 @@ cudaError_t launch_bwd_prep(const float* dy, int N, int k, const int32_t* counts
 cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* start, int E, int BM,
                                   int max_tiles, int32_t* out, cudaStream_t st);
 
-// gemm_rows.cu (tcgen05)
-cudaError_t launch_rows_gemm(int mode, bool b_mn_major, const CUtensorMap& tmap_b,
-                             const RowsParams& p, cudaStream_t st);
 // gemm_pair.cu (tcgen05, cta_group::2)
 cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_a,
                              const CUtensorMap& tmap_b, const RowsParams& p, cudaStream_t st);
 cudaError_t launch_dw_pair(const CUtensorMap& tmap_dyw, const DwParams& p, cudaStream_t st);
-// gemm_dw.cu (tcgen05)
-cudaError_t launch_dw_gemm(const CUtensorMap& tmap_dyw, const DwParams& p, cudaStream_t st);
 // gemm_masked.cu (tcgen05)
 cudaError_t launch_masked_gemm(const CUtensorMap& tmap_w, const MaskedParams& p, cudaStream_t st);
 
