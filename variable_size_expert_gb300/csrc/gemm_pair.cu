@@ -58,14 +58,16 @@ constexpr int B_STAGE = CBN * BK * 2;  // 16 KB
 constexpr int CHUNK = 64 * BK * 2;     // one 64-wide MN chunk of 64 K rows
 constexpr int NUM_THREADS = 320;
 constexpr int TMEM_COLS = 2 * PBN;
+constexpr int EPI_WARP = 32 * 32 * 4;  // one warp's 32 x 32 f32 staging block
 constexpr int NUM_BARS = 3 * STAGES + 5;
-constexpr size_t SMEM_BYTES = 1024 + static_cast<size_t>(STAGES) * (A_STAGE + B_STAGE) + 256;
+constexpr size_t SMEM_BYTES =
+    1024 + static_cast<size_t>(STAGES) * (A_STAGE + B_STAGE) + 4 * EPI_WARP + 256;
 constexpr long long DRAIN_LIMIT = 200000000LL;
 
 static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
 
 struct PairSmem {
-  uint32_t sA, sB, full, empty, gathered, acc_full, acc_empty, drain;
+  uint32_t sA, sB, sEpi, full, empty, gathered, acc_full, acc_empty, drain;
   uint32_t* tmem_slot;
   volatile int* abort_flag;
 };
@@ -77,7 +79,8 @@ __device__ __forceinline__ PairSmem carve(uint8_t* smem_raw) {
   uint8_t* gbase = smem_raw + (base - raw_addr);
   m.sA = base;
   m.sB = m.sA + STAGES * A_STAGE;
-  const uint32_t bar0 = m.sB + STAGES * B_STAGE;
+  m.sEpi = m.sB + STAGES * B_STAGE;
+  const uint32_t bar0 = m.sEpi + 4 * EPI_WARP;
   m.full = bar0;
   m.empty = bar0 + 8 * STAGES;
   m.gathered = bar0 + 16 * STAGES;
@@ -310,72 +313,115 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------ epilogue (128 threads per CTA)
-    const int r = static_cast<int>(rank) * CBM + warp * 32 + lane;  // row within the pair tile
+    // Lane i of warp w holds accumulator row 32 w + i of this CTA's half.
+    // Each 32 x 32 block passes through the warp's staging buffer (16-byte
+    // pieces XOR-swizzled by row, so both passes are free of bank
+    // conflicts) and leaves transposed: lane L then owns rows 4 j + L / 8
+    // (j = 0..7), columns 4 (L % 8) .. +3, and every store or atomic add
+    // instruction covers four rows x 128 contiguous bytes.
+    const uint32_t stg = m.sEpi + warp * EPI_WARP;
+    const int ro = static_cast<int>(rank) * CBM + warp * 32;  // first pair-tile row of the warp
+    const int kq = lane & 7;
+    const int rq = lane >> 3;
     int tcount = 0;
     for (int tau = pair; tau < total; tau += npairs) {
       const Tile t = decode_tile(tau, p.tile_start, p.start, p.E, PBM);
+      // output row and routing weight of the rows this lane stores
+      int orow[8];
+      float wgt[8];
+      {
+        const int r_own = ro + lane;
+        int o_own = t.row0 + r_own;
+        float w_own = 1.f;
+        if (MODE != kModeBare && r_own < t.rows) {
+          o_own = __ldg(p.row_token + t.row0 + r_own);
+          w_own = __ldg(p.row_weight + t.row0 + r_own);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          orow[j] = __shfl_sync(0xffffffffu, o_own, 4 * j + rq);
+          wgt[j] = __shfl_sync(0xffffffffu, w_own, 4 * j + rq);
+        }
+      }
       const int acc = tcount & 1;
       const uint32_t use = tcount >> 1;
       if (!__all_sync(0xffffffffu, wait_bar_cl(m.acc_full + 8 * acc, use & 1, wc))) break;
       tc_fence_after();
-      const bool valid = r < t.rows;
-      const int row = t.row0 + r;
-      long long orow = row;
-      float wr = 1.f;
-      if (MODE != kModeBare && valid) {
-        orow = __ldg(p.row_token + row);
-        wr = __ldg(p.row_weight + row);
-      }
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * PBN;
       const int n0 = t.nb * PBN;
-      float dot = 0.f;
+      const int nch = std::min(PBN / 32, cdiv(p.Nout - n0, 32));
+      float dot[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) dot[j] = 0.f;
+      bool released = false;
 #pragma unroll 1
-      for (int cc = 0; cc < PBN / 32; ++cc) {
-        const int col = n0 + cc * 32;
-        if (col >= p.Nout) break;  // uniform over the pair
+      for (int cc = 0; cc < nch; ++cc) {
+        const int col = n0 + cc * 32 + 4 * kq;
+        // x values of the d(routing weight) dot, requested before the
+        // accumulator block so their latency overlaps it
+        uint2 xb[8];
+        if (MODE == kModeFusedDtopk) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            xb[j] = (ro + 4 * j + rq < t.rows && col < p.Nout)
+                        ? __ldg(reinterpret_cast<const uint2*>(
+                              static_cast<const __nv_bfloat16*>(p.xdot) +
+                              static_cast<long long>(orow[j]) * p.ldx + col))
+                        : make_uint2(0u, 0u);
+        }
         float v[32];
         tmem_ld32(taddr + cc * 32, v);
         tmem_ld_wait();
-        if (valid) {
-          float* o = p.out + orow * p.ldo + col;
-          if (MODE == kModeBare) {
+        if (cc == nch - 1) {  // accumulator fully read: hand it back to the MMA
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
+          released = true;
+        }
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-              if (col + 4 * q4 < p.Nout)
-                *reinterpret_cast<float4*>(o + 4 * q4) =
-                    make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-          } else {
+        for (int k = 0; k < 8; ++k)
+          st_shared_v4(stg + lane * 128 + ((k ^ (lane & 7)) << 4), v[4 * k], v[4 * k + 1],
+                       v[4 * k + 2], v[4 * k + 3]);
+        __syncwarp();
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-              if (col + 4 * q4 < p.Nout)
-                atomicAdd(reinterpret_cast<float4*>(o + 4 * q4),
-                          make_float4(wr * v[4 * q4], wr * v[4 * q4 + 1], wr * v[4 * q4 + 2],
-                                      wr * v[4 * q4 + 3]));
-            if (MODE == kModeFusedDtopk) {
-              const __nv_bfloat16* xr =
-                  static_cast<const __nv_bfloat16*>(p.xdot) + orow * p.ldx + col;
-#pragma unroll
-              for (int q8 = 0; q8 < 4; ++q8) {
-                if (col + 8 * q8 < p.Nout) {
-                  const uint4 u = __ldg(reinterpret_cast<const uint4*>(xr + 8 * q8));
-                  const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                  for (int h = 0; h < 4; ++h) {
-                    const float lo = __uint_as_float(wds[h] << 16);
-                    const float hi = __uint_as_float(wds[h] & 0xFFFF0000u);
-                    dot = fmaf(lo, v[8 * q8 + 2 * h], dot);
-                    dot = fmaf(hi, v[8 * q8 + 2 * h + 1], dot);
-                  }
-                }
+        for (int j = 0; j < 8; ++j) {
+          const int rl = 4 * j + rq;
+          const float4 u = ld_shared_v4(stg + rl * 128 + ((kq ^ (rl & 7)) << 4));
+          if (ro + rl < t.rows && col < p.Nout) {
+            float* o = p.out + static_cast<long long>(orow[j]) * p.ldo + col;
+            if (MODE == kModeBare) {
+              *reinterpret_cast<float4*>(o) = u;
+            } else {
+              atomicAdd(reinterpret_cast<float4*>(o),
+                        make_float4(wgt[j] * u.x, wgt[j] * u.y, wgt[j] * u.z, wgt[j] * u.w));
+              if (MODE == kModeFusedDtopk) {
+                dot[j] = fmaf(__uint_as_float(xb[j].x << 16), u.x, dot[j]);
+                dot[j] = fmaf(__uint_as_float(xb[j].x & 0xFFFF0000u), u.y, dot[j]);
+                dot[j] = fmaf(__uint_as_float(xb[j].y << 16), u.z, dot[j]);
+                dot[j] = fmaf(__uint_as_float(xb[j].y & 0xFFFF0000u), u.w, dot[j]);
               }
             }
           }
         }
+        __syncwarp();  // the block is read before the next one overwrites it
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
-      if (MODE == kModeFusedDtopk && valid) atomicAdd(p.dtopk + __ldg(p.row_assign + row), dot);
+      if (!released) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
+      }
+      if (MODE == kModeFusedDtopk) {
+        // the eight lanes of a row hold partial sums over their columns
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float d = dot[j];
+          d += __shfl_xor_sync(0xffffffffu, d, 1);
+          d += __shfl_xor_sync(0xffffffffu, d, 2);
+          d += __shfl_xor_sync(0xffffffffu, d, 4);
+          const int r = ro + 4 * j + rq;
+          if (kq == 0 && r < t.rows) atomicAdd(p.dtopk + __ldg(p.row_assign + t.row0 + r), d);
+        }
+      }
       ++tcount;
     }
   }
