@@ -103,6 +103,18 @@ bool tmap_weights(CUtensorMap* m, const void* W, int E, int N, int K, int box_in
   return encode_tmap(m, W, 3, dims, strides, box);
 }
 
+// W [E][N][K] (K a multiple of 64) as the 4-D view (64, N, K/64, E): a box
+// {64, 64, 2, 1} holds 64 N-rows of two consecutive 64-wide K chunks, laid
+// out chunk after chunk as two MN-major 128-byte-swizzled blocks.
+bool tmap_weights_chunked(CUtensorMap* m, const void* W, int E, int N, int K) {
+  const uint64_t dims[4] = {64, static_cast<uint64_t>(N), static_cast<uint64_t>(K / 64),
+                            static_cast<uint64_t>(E)};
+  const uint64_t strides[3] = {static_cast<uint64_t>(K) * 2, 128,
+                               static_cast<uint64_t>(N) * K * 2};
+  const uint32_t box[4] = {64, 64, 2, 1};
+  return encode_tmap(m, W, 4, dims, strides, box);
+}
+
 // bf16 rows [rows][cols] as a 2-D tensor map, box {64 columns, box_rows rows}.
 bool tmap_rows(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
   const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
@@ -455,18 +467,33 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
                       st) != cudaSuccess)
     return MGG_ERR_CUDA;
   p.A = dy_b;
+  // dX reads W_e transposed: per stage each CTA takes 64 contraction rows of
+  // two 64-wide K chunks.  Where K is a multiple of 64 a 4-D view (64, N,
+  // K/64, E) delivers both chunks in one 16 KB box; otherwise two boxes.
   CUtensorMap tm_wt;
-  if (!tmap_weights(&tm_wt, W, E, N, K, 64, 64)) return MGG_ERR_CUDA;
+  p.b_merged = K % 64 == 0 && tmap_weights_chunked(&tm_wt, W, E, N, K);
+  if (!p.b_merged && !tmap_weights(&tm_wt, W, E, N, K, 64, 64)) return MGG_ERR_CUDA;
   if (timed(0, st, [&] { return launch_rows_pair(kModeFusedDtopk, true, tm_wt, tm_wt, p, st); }) !=
       cudaSuccess)
     return MGG_ERR_CUDA;
 
+  // dW's B operand, the scaled sorted dY [S_pad, N]: same choice over N.
   q.dyw = dyw;
   CUtensorMap tm_dyw;
-  const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(L.S_pad_max)};
-  const uint64_t strides[1] = {static_cast<uint64_t>(N) * 2};
-  const uint32_t box[2] = {64, static_cast<uint32_t>(kDwPad)};
-  if (!encode_tmap(&tm_dyw, dyw, 2, dims, strides, box)) return MGG_ERR_CUDA;
+  q.b_merged = 0;
+  if (N % 64 == 0) {
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(L.S_pad_max),
+                              static_cast<uint64_t>(N / 64)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(N) * 2, 128};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(kDwPad), 2};
+    q.b_merged = encode_tmap(&tm_dyw, dyw, 3, dims, strides, box);
+  }
+  if (!q.b_merged) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(L.S_pad_max)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(N) * 2};
+    const uint32_t box[2] = {64, static_cast<uint32_t>(kDwPad)};
+    if (!encode_tmap(&tm_dyw, dyw, 2, dims, strides, box)) return MGG_ERR_CUDA;
+  }
   return from_cuda(timed(1, st, [&] { return launch_dw_pair(tm_dyw, q, st); }));
 }
 

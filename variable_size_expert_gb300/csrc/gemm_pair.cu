@@ -181,23 +181,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const int c = q & 7;
       const int rr = q >> 3;  // this CTA's rows rr, rr+16, ..., rr+112
       const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(p.A);
+      // Row tokens of this thread's rows of a tile (-1: past the tile's
+      // rows).  The next tile's are requested while the current one runs, so
+      // the dependent loads never stall the stage that crosses the boundary.
+      auto load_tokens = [&](int tau, int(&tk)[8]) {
+        if (tau >= total) return;
+        const Tile t = decode_tile(tau, p.tile_start, p.start, p.E, PBM);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = static_cast<int>(rank) * CBM + rr + 16 * i;
+          tk[i] = r < t.rows ? __ldg(p.row_token + t.row0 + r) : -1;
+        }
+      };
+      int tok_next[8];
+      load_tokens(pair, tok_next);
       int it = 0;
       bool ok = true;
       for (int tau = pair; ok && tau < total; tau += npairs) {
-        const Tile t = decode_tile(tau, p.tile_start, p.start, p.E, PBM);
         const __nv_bfloat16* src[8];
         bool valid[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int r = static_cast<int>(rank) * CBM + rr + 16 * i;
-          valid[i] = r < t.rows;
-          const long long tok = valid[i] ? __ldg(p.row_token + t.row0 + r) : 0;
-          src[i] = A + tok * p.lda + c * 8;
+          valid[i] = tok_next[i] >= 0;
+          src[i] = A + static_cast<long long>(valid[i] ? tok_next[i] : 0) * p.lda + c * 8;
         }
+        load_tokens(tau + npairs, tok_next);
         for (int kb = 0; kb < nkb; ++kb) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!__all_sync(0xffffffffu, wait_bar_cl(m.empty + 8 * s, ph ^ 1, wc))) {
+          if (!__all_sync(0xffffffffu, wait_bar(m.empty + 8 * s, ph ^ 1, wc))) {
             ok = false;
             break;
           }
@@ -236,7 +248,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         for (int kb = 0; kb < nkb; ++kb) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!wait_bar_cl(m.empty + 8 * s, ph ^ 1, wc)) {
+          if (!wait_bar(m.empty + 8 * s, ph ^ 1, wc)) {
             ok = false;
             break;
           }
@@ -249,6 +261,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const int n0 = t.nb * PBN + static_cast<int>(rank) * CBN;
           if (!B_MN) {
             tma_load_3d_cg2(dB, &tmap_b, fb, kb * BK, n0, t.e);
+          } else if (p.b_merged) {
+            // both 64-wide chunks of this CTA's B columns in one box
+            tma_load_4d_cg2(dB, &tmap_b, fb, 0, kb * BK, n0 / 64, t.e);
           } else {
 #pragma unroll
             for (int j = 0; j < CBN / 64; ++j)
@@ -280,13 +295,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       for (int tau = pair; ok && tau < total; tau += npairs) {
         const int acc = tcount & 1;
         const uint32_t use = tcount >> 1;
-        if (!wait_bar_cl(m.acc_empty + 8 * acc, (use & 1) ^ 1, wc)) break;
+        if (!wait_bar(m.acc_empty + 8 * acc, (use & 1) ^ 1, wc)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + acc * PBN;
         for (int kb = 0; kb < nkb; ++kb) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!wait_bar_cl(m.full + 8 * s, ph, wc) ||
+          if (!wait_bar(m.full + 8 * s, ph, wc) ||
               (GATHER && !wait_bar(m.gathered + 8 * s, ph, wc))) {
             ok = false;
             break;
@@ -343,13 +358,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           wgt[j] = __shfl_sync(0xffffffffu, w_own, 4 * j + rq);
         }
       }
-      const int acc = tcount & 1;
-      const uint32_t use = tcount >> 1;
-      if (!__all_sync(0xffffffffu, wait_bar_cl(m.acc_full + 8 * acc, use & 1, wc))) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * PBN;
       const int n0 = t.nb * PBN;
       const int nch = std::min(PBN / 32, cdiv(p.Nout - n0, 32));
+      // x values of the d(routing weight) dot, fetched one 32-column block
+      // ahead (the first before the accumulator wait) to hide their latency
+      uint2 xb[8];
+      auto fetch_x = [&](int cc, uint2(&dst)[8]) {
+        const int col = n0 + cc * 32 + 4 * kq;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dst[j] = (ro + 4 * j + rq < t.rows && col < p.Nout)
+                       ? __ldg(reinterpret_cast<const uint2*>(
+                             static_cast<const __nv_bfloat16*>(p.xdot) +
+                             static_cast<long long>(orow[j]) * p.ldx + col))
+                       : make_uint2(0u, 0u);
+      };
+      if (MODE == kModeFusedDtopk) fetch_x(0, xb);
+      const int acc = tcount & 1;
+      const uint32_t use = tcount >> 1;
+      if (!__all_sync(0xffffffffu, wait_bar(m.acc_full + 8 * acc, use & 1, wc))) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * PBN;
       float dot[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) dot[j] = 0.f;
@@ -357,18 +386,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
       for (int cc = 0; cc < nch; ++cc) {
         const int col = n0 + cc * 32 + 4 * kq;
-        // x values of the d(routing weight) dot, requested before the
-        // accumulator block so their latency overlaps it
-        uint2 xb[8];
-        if (MODE == kModeFusedDtopk) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            xb[j] = (ro + 4 * j + rq < t.rows && col < p.Nout)
-                        ? __ldg(reinterpret_cast<const uint2*>(
-                              static_cast<const __nv_bfloat16*>(p.xdot) +
-                              static_cast<long long>(orow[j]) * p.ldx + col))
-                        : make_uint2(0u, 0u);
-        }
+        uint2 xn[8];
+        if (MODE == kModeFusedDtopk && cc + 1 < nch) fetch_x(cc + 1, xn);
         float v[32];
         tmem_ld32(taddr + cc * 32, v);
         tmem_ld_wait();
@@ -404,6 +423,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
         }
         __syncwarp();  // the block is read before the next one overwrites it
+        if (MODE == kModeFusedDtopk && cc + 1 < nch) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) xb[j] = xn[j];
+        }
       }
       if (!released) {
         tc_fence_before();
@@ -480,48 +503,86 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int c = q & 7;
     const int rr = q >> 3;  // rows rr + 16 i (i = 0..3) of the stage, both k chunks
     const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(p.x);
+    // Stage cursor over (tile, k-block), skipping experts with no rows.  The
+    // row tokens of a stage are fetched two stages ahead of its copies, so
+    // the dependent loads stay off the issue path.
+    struct Cur {
+      int tau, kb, nkb, m, s0, k0;
+    };
+    auto seek = [&](Cur& cu) {
+      while (cu.tau < total) {
+        const DwTile t = decode_dw(cu.tau, tiles_k, tiles_n, p.counts);
+        if (t.nkb > 0) {
+          cu.nkb = t.nkb;
+          cu.m = t.m;
+          cu.s0 = __ldg(p.start + t.e);
+          cu.k0 = t.kbo * PBM + static_cast<int>(rank) * CBM;
+          return;
+        }
+        cu.tau += npairs;
+      }
+    };
+    auto step = [&](Cur& cu) {
+      if (++cu.kb >= cu.nkb) {
+        cu.kb = 0;
+        cu.tau += npairs;
+        seek(cu);
+      }
+    };
+    auto load = [&](const Cur& cu, int(&tk)[4]) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int lr = cu.kb * BK + rr + 16 * i;
+        tk[i] = cu.tau < total && lr < cu.m ? __ldg(p.row_token + cu.s0 + lr) : -1;
+      }
+    };
+    Cur cur{pair, 0, 1, 0, 0, 0};
+    seek(cur);
+    Cur pf = cur;
+    int tk0[4], tk1[4], tk2[4];
+    load(cur, tk0);
+    step(pf);
+    load(pf, tk1);
+    step(pf);
+    load(pf, tk2);
     int it = 0;
     bool ok = true;
-    for (int tau = pair; ok && tau < total; tau += npairs) {
-      const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts);
-      const int s0 = __ldg(p.start + t.e);
-      const int k0 = t.kbo * PBM + static_cast<int>(rank) * CBM;
-      for (int kb = 0; kb < t.nkb; ++kb) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        long long tok[4];
-        bool rv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int lr = kb * BK + rr + 16 * i;
-          rv[i] = lr < t.m;
-          tok[i] = rv[i] ? __ldg(p.row_token + s0 + lr) : 0;
-        }
-        if (!__all_sync(0xffffffffu, wait_bar_cl(m.empty + 8 * s, ph ^ 1, wc))) {
-          ok = false;
-          break;
-        }
-        const uint32_t dst = m.sA + s * A_STAGE;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-#pragma unroll
-          for (int j = 0; j < CBM / 64; ++j) {
-            const int kcol = k0 + 64 * j + c * 8;
-            const bool go = rv[i] && kcol < p.K;
-            cp_async_16(dst + j * CHUNK + sw128_offset(rr + 16 * i, c),
-                        go ? static_cast<const void*>(X + tok[i] * p.K + kcol) : p.x,
-                        go ? 16u : 0u);
-          }
-        }
-        cp_async_commit();
-        if (it >= LAG) {
-          cp_async_wait<LAG>();
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(m.gathered + 8 * ((it - LAG) % STAGES));
-        }
-        ++it;
+    while (ok && cur.tau < total) {
+      const int s = it % STAGES;
+      const uint32_t ph = (it / STAGES) & 1;
+      if (!__all_sync(0xffffffffu, wait_bar(m.empty + 8 * s, ph ^ 1, wc))) {
+        ok = false;
+        break;
       }
+      const uint32_t dst = m.sA + s * A_STAGE;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int j = 0; j < CBM / 64; ++j) {
+          const int kcol = cur.k0 + 64 * j + c * 8;
+          const bool go = tk0[i] >= 0 && kcol < p.K;
+          cp_async_16(dst + j * CHUNK + sw128_offset(rr + 16 * i, c),
+                      go ? static_cast<const void*>(X + static_cast<long long>(tk0[i]) * p.K + kcol)
+                         : p.x,
+                      go ? 16u : 0u);
+        }
+      }
+      cp_async_commit();
+      if (it >= LAG) {
+        cp_async_wait<LAG>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(m.gathered + 8 * ((it - LAG) % STAGES));
+      }
+      ++it;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        tk0[i] = tk1[i];
+        tk1[i] = tk2[i];
+      }
+      step(cur);
+      step(pf);
+      load(pf, tk2);
     }
     cp_async_wait<0>();
     fence_proxy_async_smem();
@@ -540,15 +601,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         for (int kb = 0; kb < t.nkb; ++kb) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!wait_bar_cl(m.empty + 8 * s, ph ^ 1, wc)) {
+          if (!wait_bar(m.empty + 8 * s, ph ^ 1, wc)) {
             ok = false;
             break;
           }
           if (leader) mbar_arrive_expect_tx(m.full + 8 * s, 2 * B_STAGE);
           const uint32_t dB = m.sB + s * B_STAGE;
+          if (p.b_merged) {
+            // both 64-wide chunks of this CTA's n columns in one box
+            tma_load_3d_cg2(dB, &tmap_dyw, full_l + 8 * s, 0, ps + kb * BK, n0 / 64);
+          } else {
 #pragma unroll
-          for (int j = 0; j < CBN / 64; ++j)
-            tma_load_2d_cg2(dB + j * CHUNK, &tmap_dyw, full_l + 8 * s, n0 + 64 * j, ps + kb * BK);
+            for (int j = 0; j < CBN / 64; ++j)
+              tma_load_2d_cg2(dB + j * CHUNK, &tmap_dyw, full_l + 8 * s, n0 + 64 * j,
+                              ps + kb * BK);
+          }
           ++it;
         }
       }
@@ -579,13 +646,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if (t.nkb == 0) continue;
         const int acc = tcount & 1;
         const uint32_t use = tcount >> 1;
-        if (!wait_bar_cl(m.acc_empty + 8 * acc, (use & 1) ^ 1, wc)) break;
+        if (!wait_bar(m.acc_empty + 8 * acc, (use & 1) ^ 1, wc)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + acc * PBN;
         for (int kb = 0; kb < t.nkb; ++kb) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!wait_bar_cl(m.full + 8 * s, ph, wc) || !wait_bar(m.gathered + 8 * s, ph, wc)) {
+          if (!wait_bar(m.full + 8 * s, ph, wc) || !wait_bar(m.gathered + 8 * s, ph, wc)) {
             ok = false;
             break;
           }
@@ -622,7 +689,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       }
       const int acc = tcount & 1;
       const uint32_t use = tcount >> 1;
-      if (!__all_sync(0xffffffffu, wait_bar_cl(m.acc_full + 8 * acc, use & 1, wc))) break;
+      if (!__all_sync(0xffffffffu, wait_bar(m.acc_full + 8 * acc, use & 1, wc))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * PBN;
 #pragma unroll 1

@@ -43,6 +43,7 @@ struct RowsParams {
   const void* xdot;            // dtopk: x [T, ldx] (same dtype as A)
   int ldx;
   float* dtopk;                // dtopk: [S] indexed by assignment
+  int b_merged;                // MN-major B: tmap_b is the 4-D chunked view, one box per stage
   int32_t* dev_status;
   long long wait_limit;
 };
@@ -60,6 +61,7 @@ struct DwParams {
   const float* dy;             // [T, N] (f32 path)
   int E;
   float* dW;                   // [E, N, K]
+  int b_merged;                // tmap_dyw is the 3-D chunked view, one box per stage
   int32_t* dev_status;
   long long wait_limit;
 };
