@@ -305,9 +305,8 @@ def run_ours(args, ws, rank, local):
 
 def load_traffic(kernel: str):
     """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum of
-    one ncu capture, profiles/traffic.json), or None once the kernel's source
-    has changed since the capture."""
-    import hashlib
+    one ncu capture, profiles/traffic.json), or None once any source the
+    kernel is built from has changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -316,13 +315,25 @@ def load_traffic(kernel: str):
     ent = d.get(kernel)
     if not isinstance(ent, dict):
         return None
-    src = os.path.join(ROOT, "variable_size_expert_gb300", "csrc", ent.get("source", ""))
-    if not os.path.exists(src):
+    h = sources_hash(ent.get("sources", []))
+    if h is None or h != ent.get("sha256_16"):
         return None
-    with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest()[:16] != ent.get("sha256_16"):
-            return None
     return ent.get("bytes_per_launch")
+
+
+def sources_hash(names):
+    """First 16 hex digits of sha256 over the named csrc files, in order."""
+    import hashlib
+    if not names:
+        return None
+    hs = hashlib.sha256()
+    for n in names:
+        src = os.path.join(ROOT, "variable_size_expert_gb300", "csrc", n)
+        if not os.path.exists(src):
+            return None
+        with open(src, "rb") as f:
+            hs.update(f.read())
+    return hs.hexdigest()[:16]
 
 
 def run_e2e(args, p, dev, lib, mgg, L, flops_step):
