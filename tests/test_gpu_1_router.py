@@ -39,6 +39,9 @@ def _check_routing(r, ids, w, E, N):
     (1000, 8, 64, 1536, "zipf", 3),      # skewed, some experts empty
     (50, 1, 1, 8, "random", 4),          # one expert
     (2048, 4, 1024, 2048, "random", 5),  # maximum expert count, many empty
+    (8192, 4, 128, 512, "zipf", 7),      # largest single-block routing (S = 32768, E = 128)
+    (12000, 4, 64, 512, "zipf", 8),      # S above it: the multi-block router
+    (9000, 4, 129, 512, "random", 9),    # E above it: the multi-block router
 ])
 def test_route_bitexact(T, k, E, N, routing, seed):
     p = workloads.moe_problem(T=T, K=8, N=8, E=E, k=k, seed=seed, routing=routing)

@@ -360,13 +360,13 @@ mgg_status mgg_moe_forward(const void* x, const void* W, const int32_t* expert_i
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   int BM, BN;
   rows_tile(dtype, &BM, &BN);
+  // routing, and y zeroed for the epilogue's atomic adds (by the router's
+  // otherwise idle blocks where it runs as one block)
   cudaError_t e = launch_route(expert_ids, topk_weights, T, k, E, BM, cdiv(N, BN), routing->counts,
                                routing->end_offs, routing->start, routing->tile_start,
                                routing->row_assign, routing->row_token, routing->row_weight,
-                               dev_status, ws, st);
+                               dev_status, ws, st, y, static_cast<size_t>(T) * N);
   if (e != cudaSuccess) return MGG_ERR_CUDA;
-  if (cudaMemsetAsync(y, 0, static_cast<size_t>(T) * N * sizeof(float), st) != cudaSuccess)
-    return MGG_ERR_CUDA;
   RowsParams p{};
   p.A = x;
   p.lda = K;
@@ -411,12 +411,6 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   int32_t* pstart = at<int32_t>(ws, L.off_pstart);
   int BM, BN;
   rows_tile(dtype, &BM, &BN);
-  if (launch_bwd_scan(routing->counts, E, BM, cdiv(K, BN), kDwPad, tile_start_dx, pstart, st) !=
-      cudaSuccess)
-    return MGG_ERR_CUDA;
-  if (cudaMemsetAsync(dx, 0, static_cast<size_t>(T) * K * sizeof(float), st) != cudaSuccess ||
-      cudaMemsetAsync(dtopk, 0, static_cast<size_t>(T) * k * sizeof(float), st) != cudaSuccess)
-    return MGG_ERR_CUDA;
 
   RowsParams p{};
   p.lda = N;
@@ -452,6 +446,11 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   q.wait_limit = wait_limit();
 
   if (!bf) {
+    if (launch_bwd_scan(routing->counts, E, BM, cdiv(K, BN), kDwPad, tile_start_dx, pstart, st) !=
+            cudaSuccess ||
+        cudaMemsetAsync(dx, 0, static_cast<size_t>(T) * K * sizeof(float), st) != cudaSuccess ||
+        cudaMemsetAsync(dtopk, 0, static_cast<size_t>(T) * k * sizeof(float), st) != cudaSuccess)
+      return MGG_ERR_CUDA;
     p.A = dy;
     cudaError_t e = timed(0, st, [&] {
       return launch_rows_f32(kModeFusedDtopk, true, p, static_cast<const float*>(W), K, st);
@@ -462,8 +461,12 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
 
   void* dy_b = at<void>(ws, L.off_dy_b);
   void* dyw = at<void>(ws, L.off_dyw);
-  if (launch_bwd_prep(dy, N, k, routing->counts, routing->start, pstart, routing->row_token,
-                      routing->row_assign, routing->row_weight, E, L.S_pad_max, dy_b, dyw,
+  // one pass over dy: the backward schedules (dX tile prefix sums, padded
+  // segment starts), the bf16 operands of both GEMMs, and dx, dtopk zeroed
+  // for the dX epilogue's atomic adds
+  if (launch_bwd_prep(dy, N, K, k, routing->counts, routing->start, BM, cdiv(K, BN), kDwPad,
+                      tile_start_dx, pstart, routing->row_token, routing->row_assign,
+                      routing->row_weight, E, L.S_pad_max, dy_b, dyw, dx, dtopk,
                       st) != cudaSuccess)
     return MGG_ERR_CUDA;
   p.A = dy_b;

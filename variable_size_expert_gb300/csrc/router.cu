@@ -134,6 +134,99 @@ __global__ void route_scatter_kernel(const int32_t* __restrict__ ids,
   }
 }
 
+// The whole router in one block, for up to kRouteSmallS assignments and
+// kRouteSmallE experts (the three launches above cost more than the work at
+// these sizes).  Warp w owns the contiguous assignments [w*L, (w+1)*L),
+// L = ceil(S/32).  Pass 1: per-warp expert counts (lanes with the same id
+// are grouped by match.any, the group's first lane adds the group size).
+// Then counts, starts and tile prefix sums by block scans, and each warp's
+// first output row per expert = start[e] + the counts of the lower warps.
+// Pass 2: each warp walks its slice again in lane order; an assignment's row
+// is its warp's running base for the expert plus its rank among the lower
+// lanes of its group, so ties keep ascending assignment index.
+// Blocks 1.. of the launch, if any, zero `zero` (nzero4 float4s: the fused
+// forward's output, which its GEMM accumulates into) meanwhile on the other
+// SMs.
+constexpr int kRouteSmallS = 32768;
+constexpr int kRouteSmallE = 128;
+__global__ void __launch_bounds__(1024)
+    route_small_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, int S,
+                       int k, int E, int BM, int tiles_n, int32_t* __restrict__ counts,
+                       int32_t* __restrict__ end_offs, int32_t* __restrict__ start,
+                       int32_t* __restrict__ tile_start, int32_t* __restrict__ row_assign,
+                       int32_t* __restrict__ row_token, float* __restrict__ row_weight,
+                       int32_t* dev_status, float4* __restrict__ zero, long long nzero4) {
+  if (blockIdx.x > 0) {
+    const long long stride = static_cast<long long>(gridDim.x - 1) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x - 1) * blockDim.x + threadIdx.x;
+         i < nzero4; i += stride)
+      zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  __shared__ int wc[32][kRouteSmallE];  // per-warp counts, then per-warp bases
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 32 * kRouteSmallE; i += blockDim.x) (&wc[0][0])[i] = 0;
+  __syncthreads();
+  const int L = (S + 31) / 32;
+  const int a0 = warp * L, a1 = min(S, a0 + L);
+  const unsigned lt = (1u << lane) - 1u;
+  bool bad = false;
+  for (int base = a0; base < a1; base += 32) {
+    const int a = base + lane;
+    int id = a < a1 ? __ldg(ids + a) : -1;
+    if (a < a1 && (id < 0 || id >= E)) {
+      bad = true;
+      id = -1;
+    }
+    const unsigned grp = __match_any_sync(0xffffffffu, id);
+    if (id >= 0 && (grp & lt) == 0) wc[warp][id] += __popc(grp);
+    __syncwarp();  // the next group leader may be another lane
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(dev_status, kDevBadExpertId);
+  __syncthreads();
+  // per expert: total count, then (after the scans) the per-warp bases
+  const int e = threadIdx.x;
+  int m = 0;
+  if (e < E)
+    for (int v = 0; v < 32; ++v) m += wc[v][e];
+  int total_rows, total_tiles;
+  const int st = block_scan_excl(e < E ? m : 0, 0, AddOp(), &total_rows);
+  const int ts = block_scan_excl(e < E ? cdiv(m, BM) * tiles_n : 0, 0, AddOp(), &total_tiles);
+  if (e < E) {
+    counts[e] = m;
+    start[e] = st;
+    end_offs[e] = st + m;
+    tile_start[e] = ts;
+    int run = st;
+    for (int v = 0; v < 32; ++v) {
+      const int c = wc[v][e];
+      wc[v][e] = run;
+      run += c;
+    }
+  }
+  if (e == 0) {
+    start[E] = total_rows;
+    tile_start[E] = total_tiles;
+  }
+  __syncthreads();
+  for (int base = a0; base < a1; base += 32) {
+    const int a = base + lane;
+    int id = a < a1 ? __ldg(ids + a) : -1;
+    if (id >= E) id = -1;
+    const unsigned grp = __match_any_sync(0xffffffffu, id);
+    int r = 0;
+    if (id >= 0) r = wc[warp][id] + __popc(grp & lt);
+    __syncwarp();
+    if (id >= 0) {
+      if ((grp & lt) == 0) wc[warp][id] += __popc(grp);
+      row_assign[r] = a;
+      row_token[r] = a / k;
+      row_weight[r] = __ldg(w + a);
+    }
+    __syncwarp();
+  }
+}
+
 // Bare layout: caller's end offsets (or group sizes, scanned here) ->
 // clamped starts and tile prefix sums.  Offsets are made non-decreasing and
 // kept within [0, rows] so that every access stays in bounds; any repair is
@@ -196,61 +289,118 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
          (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
-// Backward operands in one pass over dy, one block per padded row p of the
+// Backward operands in one pass over dy, one warp per padded row p of the
 // scaled, expert-sorted dY operand of dW:
 //   dyw[p]   = bf16(fl32(w_r * dy[token_r]))  for the sorted row r held in p,
 //              zeros in the padding rows of each expert's segment;
 //   dy_b[t]  = bf16(dy[t]), written by the row whose assignment is token t's
-//              first (a = t*k), so every token row is written exactly once.
-// N % 8 == 0; 8 elements per thread step.
-__global__ void bwd_prep_kernel(const float* __restrict__ dy, int N, int k,
-                                const int32_t* __restrict__ counts,
-                                const int32_t* __restrict__ start,
-                                const int32_t* __restrict__ pstart,
-                                const int32_t* __restrict__ row_token,
-                                const int32_t* __restrict__ row_assign,
-                                const float* __restrict__ row_weight, int E,
-                                uint4* __restrict__ dyw, uint4* __restrict__ dy_b) {
-  const int p = blockIdx.x;
-  if (p >= __ldg(pstart + E)) return;
-  int lo = 0, hi = E + 1;  // expert whose padded segment holds p
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(pstart + mid) > p)
-      hi = mid;
-    else
-      lo = mid + 1;
+//              first (a = t*k), so every token row is written exactly once;
+//   dx[t] = 0 and dtopk[t*k .. t*k+k-1] = 0 (the dX GEMM accumulates into
+//   them), by the same row.
+// Every block derives the padded segment starts from the counts itself (a
+// block scan over at most 1024 experts) and keeps the expert tables in
+// shared memory, so the search for a row's expert costs no global round
+// trips; block 0 also publishes the padded starts and the dX tile prefix
+// sums (tiles of BM rows x tiles_n column blocks) for the GEMMs that
+// follow.  N % 8 == 0, K % 8 == 0.
+constexpr int kPrepThreads = 256;
+__global__ void __launch_bounds__(kPrepThreads)
+    bwd_prep_kernel(const float* __restrict__ dy, int N, int K, int k,
+                    const int32_t* __restrict__ counts, const int32_t* __restrict__ start,
+                    int BM, int tiles_n, int pad, int32_t* __restrict__ tile_start_dx,
+                    int32_t* __restrict__ pstart, const int32_t* __restrict__ row_token,
+                    const int32_t* __restrict__ row_assign,
+                    const float* __restrict__ row_weight, int E, uint4* __restrict__ dyw,
+                    uint4* __restrict__ dy_b, float4* __restrict__ dx, float* __restrict__ dtopk) {
+  __shared__ int s_pstart[kMaxExperts + 1];
+  __shared__ int s_start[kMaxExperts];
+  __shared__ int s_count[kMaxExperts];
+  constexpr int PER = kMaxExperts / kPrepThreads;  // experts per thread in the scans
+  {
+    int cnt[PER], psum = 0, tsum = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = threadIdx.x * PER + i;
+      cnt[i] = e < E ? __ldg(counts + e) : 0;
+      psum += cdiv(cnt[i], pad) * pad;
+      tsum += cdiv(cnt[i], BM) * tiles_n;
+    }
+    int ptot, ttot;
+    int prun = block_scan_excl(psum, 0, AddOp(), &ptot);
+    int trun = block_scan_excl(tsum, 0, AddOp(), &ttot);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = threadIdx.x * PER + i;
+      if (e < E) {
+        s_pstart[e] = prun;
+        s_start[e] = __ldg(start + e);
+        s_count[e] = cnt[i];
+        if (blockIdx.x == 0) {
+          pstart[e] = prun;
+          tile_start_dx[e] = trun;
+        }
+      }
+      prun += cdiv(cnt[i], pad) * pad;
+      trun += cdiv(cnt[i], BM) * tiles_n;
+    }
+    if (threadIdx.x == 0) {
+      s_pstart[E] = ptot;
+      if (blockIdx.x == 0) {
+        pstart[E] = ptot;
+        tile_start_dx[E] = ttot;
+      }
+    }
   }
-  const int e = lo - 1;
-  const int local = p - __ldg(pstart + e);
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int total = s_pstart[E];
   const int n8 = N / 8;
-  uint4* out = dyw + static_cast<size_t>(p) * n8;
-  if (local >= __ldg(counts + e)) {
-    for (int i = threadIdx.x; i < n8; i += blockDim.x) out[i] = make_uint4(0, 0, 0, 0);
-    return;
-  }
-  const int r = __ldg(start + e) + local;
-  const float wr = __ldg(row_weight + r);
-  const int tok = __ldg(row_token + r);
-  const bool first = __ldg(row_assign + r) % k == 0;
-  const float4* src = reinterpret_cast<const float4*>(dy + static_cast<size_t>(tok) * N);
-  uint4* outb = dy_b + static_cast<size_t>(tok) * n8;
-  for (int i = threadIdx.x; i < n8; i += blockDim.x) {
-    const float4 a = src[2 * i];
-    const float4 b = src[2 * i + 1];
-    uint4 o;
-    o.x = pack_bf16x2(__fmul_rn(wr, a.x), __fmul_rn(wr, a.y));
-    o.y = pack_bf16x2(__fmul_rn(wr, a.z), __fmul_rn(wr, a.w));
-    o.z = pack_bf16x2(__fmul_rn(wr, b.x), __fmul_rn(wr, b.y));
-    o.w = pack_bf16x2(__fmul_rn(wr, b.z), __fmul_rn(wr, b.w));
-    out[i] = o;
+  for (int p = blockIdx.x * wpb + (threadIdx.x >> 5); p < total; p += gridDim.x * wpb) {
+    int lo = 0, hi = E + 1;  // expert whose padded segment holds p
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_pstart[mid] > p)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    const int e = lo - 1;
+    const int local = p - s_pstart[e];
+    uint4* out = dyw + static_cast<size_t>(p) * n8;
+    if (local >= s_count[e]) {
+      for (int i = lane; i < n8; i += 32) out[i] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const int r = s_start[e] + local;
+    const float wr = __ldg(row_weight + r);
+    const int tok = __ldg(row_token + r);
+    const bool first = __ldg(row_assign + r) % k == 0;
+    const float4* src = reinterpret_cast<const float4*>(dy + static_cast<size_t>(tok) * N);
+    uint4* outb = dy_b + static_cast<size_t>(tok) * n8;
+#pragma unroll 4
+    for (int i = lane; i < n8; i += 32) {
+      const float4 a = __ldg(src + 2 * i);
+      const float4 b = __ldg(src + 2 * i + 1);
+      uint4 o;
+      o.x = pack_bf16x2(__fmul_rn(wr, a.x), __fmul_rn(wr, a.y));
+      o.y = pack_bf16x2(__fmul_rn(wr, a.z), __fmul_rn(wr, a.w));
+      o.z = pack_bf16x2(__fmul_rn(wr, b.x), __fmul_rn(wr, b.y));
+      o.w = pack_bf16x2(__fmul_rn(wr, b.z), __fmul_rn(wr, b.w));
+      out[i] = o;
+      if (first) {
+        uint4 q;
+        q.x = pack_bf16x2(a.x, a.y);
+        q.y = pack_bf16x2(a.z, a.w);
+        q.z = pack_bf16x2(b.x, b.y);
+        q.w = pack_bf16x2(b.z, b.w);
+        outb[i] = q;
+      }
+    }
     if (first) {
-      uint4 q;
-      q.x = pack_bf16x2(a.x, a.y);
-      q.y = pack_bf16x2(a.z, a.w);
-      q.z = pack_bf16x2(b.x, b.y);
-      q.w = pack_bf16x2(b.z, b.w);
-      outb[i] = q;
+      float4* dxr = dx + static_cast<size_t>(tok) * (K / 4);
+      for (int i = lane; i < K / 4; i += 32) dxr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = lane; j < k; j += 32) dtopk[static_cast<size_t>(tok) * k + j] = 0.f;
     }
   }
 }
@@ -282,8 +432,27 @@ size_t route_ws_bytes(int T, int k, int E) {
 cudaError_t launch_route(const int32_t* ids, const float* w, int T, int k, int E, int BM,
                          int tiles_n, int32_t* counts, int32_t* end_offs, int32_t* start,
                          int32_t* tile_start, int32_t* row_assign, int32_t* row_token,
-                         float* row_weight, int32_t* dev_status, void* ws, cudaStream_t st) {
+                         float* row_weight, int32_t* dev_status, void* ws, cudaStream_t st,
+                         float* zero, size_t zero_floats) {
   const int S = T * k;
+  // the single-block router zeroes `zero` with its other blocks (float4 at a
+  // time: needs 16-byte alignment and a multiple of 4 floats)
+  const bool fuse_zero = zero && zero_floats % 4 == 0 && reinterpret_cast<uintptr_t>(zero) % 16 == 0;
+  if (S <= kRouteSmallS && E <= kRouteSmallE) {
+    const int blocks = 1 + (fuse_zero && zero_floats > 0 ? std::max(1, num_sms() - 1) : 0);
+    route_small_kernel<<<blocks, 1024, 0, st>>>(
+        ids, w, S, k, E, BM, tiles_n, counts, end_offs, start, tile_start, row_assign, row_token,
+        row_weight, dev_status, reinterpret_cast<float4*>(zero),
+        fuse_zero ? static_cast<long long>(zero_floats / 4) : 0);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess && zero && !fuse_zero && zero_floats > 0)
+      e = cudaMemsetAsync(zero, 0, zero_floats * sizeof(float), st);
+    return e;
+  }
+  if (zero && zero_floats > 0) {
+    cudaError_t e = cudaMemsetAsync(zero, 0, zero_floats * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
   const int nchunks = (S + kRouteChunk - 1) / kRouteChunk;
   int32_t* chunk = static_cast<int32_t*>(ws);
   route_hist_kernel<<<nchunks, kRouteChunk, 0, st>>>(ids, S, E, chunk, dev_status);
@@ -308,14 +477,18 @@ cudaError_t launch_bwd_scan(const int32_t* counts, int E, int BM, int tiles_n, i
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_prep(const float* dy, int N, int k, const int32_t* counts,
-                            const int32_t* start, const int32_t* pstart, const int32_t* row_token,
+cudaError_t launch_bwd_prep(const float* dy, int N, int K, int k, const int32_t* counts,
+                            const int32_t* start, int BM, int tiles_n, int pad,
+                            int32_t* tile_start_dx, int32_t* pstart, const int32_t* row_token,
                             const int32_t* row_assign, const float* row_weight, int E,
-                            int S_pad_max, void* dy_b, void* dyw, cudaStream_t st) {
-  if (S_pad_max > 0)
-    bwd_prep_kernel<<<S_pad_max, 256, 0, st>>>(dy, N, k, counts, start, pstart, row_token,
-                                               row_assign, row_weight, E,
-                                               static_cast<uint4*>(dyw), static_cast<uint4*>(dy_b));
+                            int S_pad_max, void* dy_b, void* dyw, float* dx, float* dtopk,
+                            cudaStream_t st) {
+  const int wpb = kPrepThreads / 32;
+  const int blocks = std::max(1, std::min(cdiv(S_pad_max, wpb), num_sms() * (2048 / kPrepThreads)));
+  bwd_prep_kernel<<<blocks, kPrepThreads, 0, st>>>(
+      dy, N, K, k, counts, start, BM, tiles_n, pad, tile_start_dx, pstart, row_token, row_assign,
+      row_weight, E,
+      static_cast<uint4*>(dyw), static_cast<uint4*>(dy_b), reinterpret_cast<float4*>(dx), dtopk);
   return cudaGetLastError();
 }
 
