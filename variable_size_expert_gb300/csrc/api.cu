@@ -200,6 +200,22 @@ bool encode_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* d
   return r == CUDA_SUCCESS;
 }
 
+// f32 [E][N][K] (dW) as a 3-D map for TMA tile stores, box {128, 32, 1}, no
+// swizzle: the staged block is row-major like the tensor.
+bool tmap_dw_store(CUtensorMap* map, float* dW, int E, int N, int K) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tmap_encoder();
+  if (!fn) return false;
+  cuuint64_t d[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
+                     static_cast<cuuint64_t>(E)};
+  cuuint64_t st[2] = {static_cast<cuuint64_t>(K) * 4, static_cast<cuuint64_t>(N) * K * 4};
+  cuuint32_t b[3] = {128, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dW, d, st, b, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace mgg
 
 using namespace mgg;
@@ -400,7 +416,7 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   if (s != MGG_OK) return s;
   const bool bf = dtype == MGG_BF16;
   if (!aligned(x, bf ? 16 : 4) || !aligned(W, bf ? 16 : 4) || !aligned(dy, bf ? 16 : 4) ||
-      !aligned(dx, bf ? 16 : 4) || !aligned(dW, 4) || !aligned(dtopk, 4))
+      !aligned(dx, bf ? 16 : 4) || !aligned(dW, bf ? 16 : 4) || !aligned(dtopk, 4))
     return MGG_ERR_ALIGNMENT;
   const BwdLayout L = bwd_layout(T, k, E, N, K, dtype);
   if (ws_bytes < L.total || !aligned(ws, 256)) return MGG_ERR_WORKSPACE;
@@ -497,7 +513,9 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
     const uint32_t box[2] = {64, static_cast<uint32_t>(kDwPad)};
     if (!encode_tmap(&tm_dyw, dyw, 2, dims, strides, box)) return MGG_ERR_CUDA;
   }
-  return from_cuda(timed(1, st, [&] { return launch_dw_pair(tm_dyw, q, st); }));
+  CUtensorMap tm_dw;
+  if (!tmap_dw_store(&tm_dw, dW, E, N, K)) return MGG_ERR_CUDA;
+  return from_cuda(timed(1, st, [&] { return launch_dw_pair(tm_dyw, tm_dw, q, st); }));
 }
 
 mgg_status mgg_debug_tile_schedule(const mgg_routing* routing, int E, int N, mgg_dtype dtype,

@@ -51,20 +51,28 @@ constexpr int CBM = PBM / 2;   // rows per CTA
 constexpr int PBN = kPairBN;   // columns of a pair tile (MMA N)
 constexpr int CBN = PBN / 2;   // B rows per CTA
 constexpr int BK = kBK;
-constexpr int STAGES = 6;
-constexpr int LAG = 3;         // cp.async groups a gather thread keeps in flight (< STAGES)
+constexpr int kRowsStages = 6;  // + 16 KB of epilogue staging (4 warps x 32 x 32 f32)
+constexpr int kDwStages = 6;    // + 32 KB: two 32 (n) x 128 (k) f32 blocks for the TMA store
+constexpr int LAG = 3;          // cp.async groups a gather thread keeps in flight (< stages)
 constexpr int A_STAGE = CBM * BK * 2;  // 16 KB
 constexpr int B_STAGE = CBN * BK * 2;  // 16 KB
 constexpr int CHUNK = 64 * BK * 2;     // one 64-wide MN chunk of 64 K rows
 constexpr int NUM_THREADS = 320;
 constexpr int TMEM_COLS = 2 * PBN;
 constexpr int EPI_WARP = 32 * 32 * 4;  // one warp's 32 x 32 f32 staging block
-constexpr int NUM_BARS = 3 * STAGES + 5;
-constexpr size_t SMEM_BYTES =
-    1024 + static_cast<size_t>(STAGES) * (A_STAGE + B_STAGE) + 4 * EPI_WARP + 256;
+constexpr int kRowsEpi = 4 * EPI_WARP;
+constexpr int DW_EPI_BUF = 32 * CBM * 4;  // one 32 (n) x 128 (k) f32 block
+constexpr int kDwEpi = 2 * DW_EPI_BUF;
+constexpr int kBarBytes = 256;
+template <int STAGES, int EPI_BYTES>
+constexpr size_t smem_bytes() {
+  return 1024 + static_cast<size_t>(STAGES) * (A_STAGE + B_STAGE) + EPI_BYTES + kBarBytes;
+}
+static_assert(smem_bytes<kRowsStages, kRowsEpi>() <= 232448 &&
+                  smem_bytes<kDwStages, kDwEpi>() <= 232448,
+              "shared memory per block");
 constexpr long long DRAIN_LIMIT = 200000000LL;
 
-static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
 
 struct PairSmem {
   uint32_t sA, sB, sEpi, full, empty, gathered, acc_full, acc_empty, drain;
@@ -72,7 +80,10 @@ struct PairSmem {
   volatile int* abort_flag;
 };
 
+template <int STAGES, int EPI_BYTES>
 __device__ __forceinline__ PairSmem carve(uint8_t* smem_raw) {
+  constexpr int NUM_BARS = 3 * STAGES + 5;
+  static_assert(NUM_BARS * 8 + 8 <= kBarBytes, "barrier area");
   PairSmem m;
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -80,7 +91,7 @@ __device__ __forceinline__ PairSmem carve(uint8_t* smem_raw) {
   m.sA = base;
   m.sB = m.sA + STAGES * A_STAGE;
   m.sEpi = m.sB + STAGES * B_STAGE;
-  const uint32_t bar0 = m.sEpi + 4 * EPI_WARP;
+  const uint32_t bar0 = m.sEpi + EPI_BYTES;
   m.full = bar0;
   m.empty = bar0 + 8 * STAGES;
   m.gathered = bar0 + 16 * STAGES;
@@ -101,6 +112,7 @@ __device__ __forceinline__ PairSmem carve(uint8_t* smem_raw) {
 // local phase, so the forward carries no release fence: a release at cluster
 // scope costs a memory barrier per stage and measured 1.5x slower overall.
 // The leader's MMA thread waits on its own gathered[s] directly.
+template <int STAGES>
 __device__ __forceinline__ bool relay_stage(const PairSmem& m, uint32_t full_l, int it,
                                             const WaitCtl& wc) {
   const int s = it % STAGES;
@@ -108,9 +120,10 @@ __device__ __forceinline__ bool relay_stage(const PairSmem& m, uint32_t full_l, 
   mbar_arrive_cluster_relaxed(full_l + 8 * s);
   return true;
 }
-static_assert(LAG < STAGES, "gather lag must be below the ring depth");
+static_assert(LAG < kRowsStages && LAG < kDwStages, "gather lag must be below the ring depth");
 
 // Barrier set-up, TMEM allocation on both CTAs, cluster-wide handshake.
+template <int STAGES>
 __device__ __forceinline__ uint32_t pair_setup(const PairSmem& m, uint32_t full_count, int warp) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -154,7 +167,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                      const __grid_constant__ CUtensorMap tmap_b, const RowsParams p) {
   constexpr bool GATHER = MODE != kModeBare;
   extern __shared__ uint8_t smem_raw[];
-  const PairSmem m = carve(smem_raw);
+  constexpr int STAGES = kRowsStages;
+  const PairSmem m = carve<STAGES, kRowsEpi>(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -166,7 +180,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (!GATHER) tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
   }
-  const uint32_t tmem_base = pair_setup(m, GATHER ? 2 : 1, warp);
+  const uint32_t tmem_base = pair_setup<STAGES>(m, GATHER ? 2 : 1, warp);
   const uint32_t full_l = mapa_shared(m.full, 0);           // leader's full[0]
   const uint32_t acc_empty_l = mapa_shared(m.acc_empty, 0);  // leader's acc_empty[0]
 
@@ -283,7 +297,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int tau = pair; ok && tau < total; tau += npairs)
         for (int kb = 0; kb < nkb; ++kb, ++it)
-          if (!relay_stage(m, full_l, it, wc)) {
+          if (!relay_stage<STAGES>(m, full_l, it, wc)) {
             ok = false;
             break;
           }
@@ -477,9 +491,11 @@ __device__ __forceinline__ DwTile decode_dw(int tau, int tiles_k, int tiles_n,
 // by TMA.  Rows past m_e are zero-filled on the x side and zero-padded on
 // the dY side.  Tiles of experts with no rows write zeros.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    dw_pair_kernel(const __grid_constant__ CUtensorMap tmap_dyw, const DwParams p) {
+    dw_pair_kernel(const __grid_constant__ CUtensorMap tmap_dyw,
+                   const __grid_constant__ CUtensorMap tmap_dw, const DwParams p) {
   extern __shared__ uint8_t smem_raw[];
-  const PairSmem m = carve(smem_raw);
+  constexpr int STAGES = kDwStages;
+  const PairSmem m = carve<STAGES, kDwEpi>(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -488,7 +504,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const int npairs = gridDim.x >> 1;
 
   if (warp == 5 && lane == 0) tma_prefetch_desc(&tmap_dyw);
-  const uint32_t tmem_base = pair_setup(m, 2, warp);
+  if (threadIdx.x == 0) tma_prefetch_desc(&tmap_dw);
+  const uint32_t tmem_base = pair_setup<STAGES>(m, 2, warp);
   const uint32_t full_l = mapa_shared(m.full, 0);
   const uint32_t acc_empty_l = mapa_shared(m.acc_empty, 0);
 
@@ -631,7 +648,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       for (int tau = pair; ok && tau < total; tau += npairs) {
         const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts);
         for (int kb = 0; kb < t.nkb; ++kb, ++it)
-          if (!relay_stage(m, full_l, it, wc)) {
+          if (!relay_stage<STAGES>(m, full_l, it, wc)) {
             ok = false;
             break;
           }
@@ -675,41 +692,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------ epilogue (128 threads per CTA)
-    int tcount = 0;
+    // Lane i of warp w holds dW column k = k0 + 32 w + i (TMEM lane), 32
+    // output rows n per block.  The four warps write each 32 (n) x 128 (k)
+    // block into one of two staging buffers, row-major like dW itself, and
+    // thread 0 stores it with one TMA tile store (clipped at N and K), so
+    // the output leaves without load/store-unit traffic.  Named barrier 1
+    // (these 128 threads) orders the buffer hand-offs; the tile loop's one
+    // wait is taken as a single decision of all four warps.
+    const bool issuer = threadIdx.x == 0;
+    int tcount = 0, nst = 0;
     for (int tau = pair; tau < total; tau += npairs) {
       const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts);
-      const int kcol = t.kbo * PBM + static_cast<int>(rank) * CBM + warp * 32 + lane;
-      float* out = p.dW + static_cast<size_t>(t.e) * p.N * p.K + kcol;
+      const int k0 = t.kbo * PBM + static_cast<int>(rank) * CBM;
+      const int kcol = k0 + warp * 32 + lane;
       const int n0 = t.nb * PBN;
       if (t.nkb == 0) {
         // expert with no rows: its gradient is exactly zero, and is written
+        float* out = p.dW + static_cast<size_t>(t.e) * p.N * p.K + kcol;
         if (kcol < p.K)
           for (int n = n0; n < min(n0 + PBN, p.N); ++n) out[static_cast<size_t>(n) * p.K] = 0.f;
         continue;
       }
       const int acc = tcount & 1;
       const uint32_t use = tcount >> 1;
-      if (!__all_sync(0xffffffffu, wait_bar(m.acc_full + 8 * acc, use & 1, wc))) break;
+      if (!bar_and(1, 128, wait_bar(m.acc_full + 8 * acc, use & 1, wc))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * PBN;
+      const int nch = std::min(PBN / 32, cdiv(p.N - n0, 32));
 #pragma unroll 1
-      for (int cc = 0; cc < PBN / 32; ++cc) {
-        const int n = n0 + cc * 32;
-        if (n >= p.N) break;
+      for (int cc = 0; cc < nch; ++cc) {
         float v[32];
         tmem_ld32(taddr + cc * 32, v);
         tmem_ld_wait();
-        if (kcol < p.K) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (n + i < p.N) out[static_cast<size_t>(n + i) * p.K] = v[i];
+        if (cc == nch - 1) {  // accumulator fully read: hand it back to the MMA
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
         }
+        const uint32_t buf = m.sEpi + (nst & 1) * DW_EPI_BUF;
+        if (issuer) bulk_wait_read<1>();  // the store two blocks ago has read this buffer
+        bar_named(1, 128);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) st_shared_f32(buf + i * (CBM * 4) + (warp * 32 + lane) * 4, v[i]);
+        fence_proxy_async_smem();
+        bar_named(1, 128);
+        if (issuer && k0 < p.K) {  // (a block wholly past K is not stored)
+          tma_store_3d(&tmap_dw, buf, k0, n0 + cc * 32, t.e);
+          bulk_commit();
+        }
+        ++nst;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
       ++tcount;
     }
+    if (issuer) bulk_wait<0>();
   }
 
   pair_teardown(tmem_base, warp);
@@ -718,7 +753,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 // Largest grid of co-resident pairs (a persistent kernel must not have
 // clusters waiting for others to finish).
 template <typename K>
-int pair_grid(K kern) {
+int pair_grid(K kern, size_t smem) {
   static int cache[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -726,7 +761,7 @@ int pair_grid(K kern) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms() & ~1, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
   attr.val.clusterDim.x = 2;
@@ -743,12 +778,12 @@ int pair_grid(K kern) {
 }
 
 template <typename K>
-cudaError_t prepare(K kern, bool* done) {
+cudaError_t prepare(K kern, size_t smem, bool* done) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && done[dev]) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(SMEM_BYTES));
+                                       static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (dev < 64) done[dev] = true;
   return cudaSuccess;
@@ -759,9 +794,10 @@ cudaError_t launch_rows_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
                                cudaStream_t st) {
   auto kern = rows_pair_kernel<MODE, B_MN>;
   static bool done[64] = {};
-  cudaError_t e = prepare(kern, done);
+  constexpr size_t smem = smem_bytes<kRowsStages, kRowsEpi>();
+  cudaError_t e = prepare(kern, smem, done);
   if (e != cudaSuccess) return e;
-  kern<<<pair_grid(kern), NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+  kern<<<pair_grid(kern, smem), NUM_THREADS, smem, st>>>(ta, tb, p);
   return cudaGetLastError();
 }
 
@@ -779,11 +815,13 @@ cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_dw_pair(const CUtensorMap& tmap_dyw, const DwParams& p, cudaStream_t st) {
+cudaError_t launch_dw_pair(const CUtensorMap& tmap_dyw, const CUtensorMap& tmap_dw,
+                           const DwParams& p, cudaStream_t st) {
   static bool done[64] = {};
-  cudaError_t e = prepare(dw_pair_kernel, done);
+  constexpr size_t smem = smem_bytes<kDwStages, kDwEpi>();
+  cudaError_t e = prepare(dw_pair_kernel, smem, done);
   if (e != cudaSuccess) return e;
-  dw_pair_kernel<<<pair_grid(dw_pair_kernel), NUM_THREADS, SMEM_BYTES, st>>>(tmap_dyw, p);
+  dw_pair_kernel<<<pair_grid(dw_pair_kernel, smem), NUM_THREADS, smem, st>>>(tmap_dyw, tmap_dw, p);
   return cudaGetLastError();
 }
 
