@@ -187,6 +187,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const WaitCtl wc{m.abort_flag, p.dev_status, p.wait_limit};
   const int total = __ldg(p.tile_start + p.E);
   const int nkb = cdiv(p.Kc, BK);
+  // The column halves of the last round pay off only where A arrives by TMA:
+  // a half still needs all 256 gathered rows, and in the gather modes the
+  // halves measured slower than the idle round they replace.
+  constexpr bool SPLIT = !GATHER;
+  const WorkPlan plan = work_plan(pair, npairs, total, SPLIT);
+  const int nwork = plan.count();
+  // Every role walks (wi, tau) together; without the split the work item is
+  // just the tile tau and the plan folds away.
+  auto more = [&](int wi, int tau) { return SPLIT ? wi < nwork : tau < total; };
+  auto item = [&](int wi, int tau) { return SPLIT ? plan.get(wi) : WorkItem{tau, 0, 1}; };
 
   if (warp >= 6) {
     // ------------------------------------------------ A gather (128 threads per CTA)
@@ -211,6 +221,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       load_tokens(pair, tok_next);
       int it = 0;
       bool ok = true;
+      static_assert(!SPLIT || !GATHER, "the gather walks whole tiles only");
       for (int tau = pair; ok && tau < total; tau += npairs) {
         const __nv_bfloat16* src[8];
         bool valid[8];
@@ -254,11 +265,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 5) {
     // ------------------------------------------------ TMA: B half (+ A half in bare mode)
     if (lane == 0) {
-      constexpr uint32_t TX = 2 * (B_STAGE + (GATHER ? 0 : A_STAGE));  // both CTAs
       int it = 0;
       bool ok = true;
-      for (int tau = pair; ok && tau < total; tau += npairs) {
-        const Tile t = decode_tile(tau, p.tile_start, p.start, p.E, PBM);
+      constexpr uint32_t TX = 2 * (B_STAGE + (GATHER ? 0 : A_STAGE));  // both CTAs
+      for (int wi = 0, tau = pair; ok && more(wi, tau); ++wi, tau += npairs) {
+        const WorkItem w = item(wi, tau);
+        const Tile t = decode_tile(w.tau, p.tile_start, p.start, p.E, PBM);
         for (int kb = 0; kb < nkb; ++kb) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -273,7 +285,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                             t.row0 + static_cast<int>(rank) * CBM);
           const uint32_t dB = m.sB + s * B_STAGE;
           const int n0 = t.nb * PBN + static_cast<int>(rank) * CBN;
-          if (!B_MN) {
+          if (SPLIT && w.nhalves == 2) {
+            // a half's 64 B rows are the first 64 of a 128-row box at a
+            // shifted row (the other 64 are loaded and not read)
+            const int nh = t.nb * PBN + w.half * (PBN / 2) + static_cast<int>(rank) * (CBN / 2);
+            tma_load_3d_cg2(dB, &tmap_b, fb, kb * BK, nh, t.e);
+          } else if (!B_MN) {
             tma_load_3d_cg2(dB, &tmap_b, fb, kb * BK, n0, t.e);
           } else if (p.b_merged) {
             // both 64-wide chunks of this CTA's B columns in one box
@@ -295,7 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (!leader && GATHER && lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int tau = pair; ok && tau < total; tau += npairs)
+      for (int wi = 0, tau = pair; ok && more(wi, tau); ++wi, tau += npairs)
         for (int kb = 0; kb < nkb; ++kb, ++it)
           if (!relay_stage<STAGES>(m, full_l, it, wc)) {
             ok = false;
@@ -304,9 +321,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     if (leader && lane == 0) {
       constexpr uint32_t IDESC = idesc_bf16_f32(PBM, PBN, false, B_MN);
+      constexpr uint32_t IDESC_H = idesc_bf16_f32(PBM, PBN / 2, false, B_MN);
       int it = 0, tcount = 0;
       bool ok = true;
-      for (int tau = pair; ok && tau < total; tau += npairs) {
+      for (int wi = 0, tau = pair; ok && more(wi, tau); ++wi, tau += npairs) {
+        const uint32_t idesc = SPLIT && item(wi, tau).nhalves == 2 ? IDESC_H : IDESC;
         const int acc = tcount & 1;
         const uint32_t use = tcount >> 1;
         if (!wait_bar(m.acc_empty + 8 * acc, (use & 1) ^ 1, wc)) break;
@@ -328,7 +347,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             const uint64_t adesc = sw128_desc(a0 + kk * 32, 16, 1024);
             const uint64_t bdesc = B_MN ? sw128_desc(b0 + kk * 16 * 128, CHUNK, 1024)
                                         : sw128_desc(b0 + kk * 32, 16, 1024);
-            tc_mma_bf16_cg2(d, adesc, bdesc, IDESC, (kb | kk) != 0);
+            tc_mma_bf16_cg2(d, adesc, bdesc, idesc, (kb | kk) != 0);
           }
           tc_commit_cg2_mc(m.empty + 8 * s, 0x3);
           ++it;
@@ -353,8 +372,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int kq = lane & 7;
     const int rq = lane >> 3;
     int tcount = 0;
-    for (int tau = pair; tau < total; tau += npairs) {
-      const Tile t = decode_tile(tau, p.tile_start, p.start, p.E, PBM);
+    for (int wi = 0, tau = pair; more(wi, tau); ++wi, tau += npairs) {
+      const WorkItem w = item(wi, tau);
+      const Tile t = decode_tile(w.tau, p.tile_start, p.start, p.E, PBM);
       // output row and routing weight of the rows this lane stores
       int orow[8];
       float wgt[8];
@@ -372,8 +392,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           wgt[j] = __shfl_sync(0xffffffffu, w_own, 4 * j + rq);
         }
       }
-      const int n0 = t.nb * PBN;
-      const int nch = std::min(PBN / 32, cdiv(p.Nout - n0, 32));
+      const int n0 = t.nb * PBN + (SPLIT ? w.half * (PBN / 2) : 0);
+      const int nch =
+          std::min((SPLIT && w.nhalves == 2 ? PBN / 2 : PBN) / 32, cdiv(p.Nout - n0, 32));
       // x values of the d(routing weight) dot, fetched one 32-column block
       // ahead (the first before the accumulator wait) to hide their latency
       uint2 xb[8];

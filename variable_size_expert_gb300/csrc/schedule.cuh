@@ -43,4 +43,39 @@ __device__ __forceinline__ Tile decode_tile(int tau, const int32_t* __restrict__
   return t;
 }
 
+// The work of persistent worker w (of W) over `total` tiles.  Whole tiles go
+// round-robin.  When the last round would leave more than half of the
+// workers idle (0 < total mod W <= W/2), its tiles are cut instead into two
+// halves along the output columns, one half per worker, so that round takes
+// about half as long when the round is bound by the tensor cores and the
+// tile's A rows are cheap to fetch twice.  Every output element is still
+// produced by exactly one tile (or half), so the split changes no result.
+struct WorkItem {
+  int tau;      // tile
+  int half;     // column half (0 for a whole tile)
+  int nhalves;  // 1: whole tile; 2: half `half` of its columns
+};
+
+struct WorkPlan {
+  int w, W, whole, nwhole, nsplit;
+
+  __device__ __forceinline__ int count() const { return nwhole + (w < nsplit ? 1 : 0); }
+  __device__ __forceinline__ WorkItem get(int i) const {
+    if (i < nwhole) return WorkItem{w + i * W, 0, 1};
+    return WorkItem{whole + (w >> 1), w & 1, 2};
+  }
+};
+
+__device__ __forceinline__ WorkPlan work_plan(int w, int W, int total, bool allow_split) {
+  const int R = total % W;
+  const bool split = allow_split && R > 0 && 2 * R <= W;
+  WorkPlan pl;
+  pl.w = w;
+  pl.W = W;
+  pl.whole = total - (split ? R : 0);
+  pl.nwhole = pl.whole > w ? (pl.whole - w + W - 1) / W : 0;
+  pl.nsplit = split ? 2 * R : 0;
+  return pl;
+}
+
 }  // namespace mgg
