@@ -27,7 +27,7 @@ __all__ = [
     "bf16_round", "fp32_mul", "Routing", "route", "end_offsets", "tile_schedule",
     "schedule_stats", "grouped_gemm", "moe_forward", "moe_forward_unfused",
     "moe_backward", "moe_backward_rows", "moe_backward_dw_rows", "masked_grouped_gemm",
-    "moe_loss", "rel_frobenius", "max_abs_ratio",
+    "moe_loss", "rel_frobenius", "max_abs_ratio", "silu", "moe_ffn_forward",
 ]
 
 
@@ -325,6 +325,57 @@ def moe_backward_dw_rows(dy, x, W, expert_ids, topk_weights, pairs, bf16_operand
         a = _dyw_operand(w[t, j], dy32[t, n][:, None], bf16_operands)[:, 0]
         out[i] = a @ x[t]
     return out
+
+
+# --------------------------------------------------------------------------
+# Gated expert FFN forward  [P1 §Choosing an implementation]
+# --------------------------------------------------------------------------
+def silu(a) -> np.ndarray:
+    """SiLU, a * sigmoid(a) = a / (1 + exp(-a)), in float64."""
+    a = np.asarray(a, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return a / (1.0 + np.exp(-a))
+
+
+def moe_ffn_forward(x, Wg, Wu, Wd, expert_ids, topk_weights, tokens=None, round_h=True):
+    """One gated MoE FFN layer, per assignment a = (t, j), e = ids[t, j]:
+
+        g   = x[t] Wg_e^T,  u = x[t] Wu_e^T        gate and up projections [F]
+        h_a = bf16(silu(g) * u)                     gated activation
+        y[t] += w[t, j] * h_a Wd_e^T               down projection, top-k combine
+
+    P1 names the gated FFN (two up-projections, gate and up, as one grouped
+    GEMM with N doubled, then an activation in the epilogue) without naming
+    the activation; SiLU gating (SwiGLU) is the reading taken here.  h is the
+    bfloat16 operand of the down-projection GEMM, hence its rounding
+    (``round_h=False`` returns the float64 value before it).  Weights are
+    stored like nn.Linear: Wg, Wu [E, F, H], Wd [E, H, F].
+
+    Returns (y [n, H], h [n, k, F]) for the n token rows of ``tokens`` (all
+    tokens by default), h in assignment order (t, j).
+    """
+    ids = np.asarray(expert_ids)
+    w = np.asarray(topk_weights, dtype=np.float64)
+    x = np.asarray(x, dtype=np.float64)
+    tok = np.arange(ids.shape[0]) if tokens is None else np.asarray(tokens)
+    k = ids.shape[1]
+    F, H = Wg.shape[1], Wd.shape[1]
+    y = np.zeros((tok.size, H))
+    h = np.zeros((tok.size, k, F))
+    for j in range(k):
+        for e in range(Wg.shape[0]):
+            sel = np.nonzero(ids[tok, j] == e)[0]
+            if not sel.size:
+                continue
+            xt = x[tok[sel]]
+            g = xt @ np.asarray(Wg[e], dtype=np.float64).T
+            u = xt @ np.asarray(Wu[e], dtype=np.float64).T
+            ha = silu(g) * u
+            if round_h:
+                ha = bf16_round(ha)
+            h[sel, j] = ha
+            y[sel] += w[tok[sel], j][:, None] * (ha @ np.asarray(Wd[e], dtype=np.float64).T)
+    return y, h
 
 
 # --------------------------------------------------------------------------

@@ -458,6 +458,79 @@ def test_error_measures():
 
 
 # ---------------------------------------------------------------- planted mistakes
+# ---------------------------------------------------------------- gated FFN
+def _brute_ffn_pre(x, Wg, Wu, ids):
+    """Pure-Python loops: g, u dot products per assignment and feature, SiLU
+    by math.exp, their product (before the bfloat16 rounding of h)."""
+    T, k, F, H = len(ids), len(ids[0]), len(Wg[0]), len(x[0])
+    out = [[[0.0] * F for _ in range(k)] for _ in range(T)]
+    for t in range(T):
+        for j in range(k):
+            e = ids[t][j]
+            for f in range(F):
+                g = sum(x[t][c] * Wg[e][f][c] for c in range(H))
+                u = sum(x[t][c] * Wu[e][f][c] for c in range(H))
+                out[t][j][f] = g / (1.0 + math.exp(-g)) * u
+    return np.array(out)
+
+
+def _brute_ffn_down(h, Wd, ids, w):
+    """Pure-Python loops: y[t] = sum_j w[t][j] * h[t][j] Wd_e^T."""
+    T, k, F, H = len(ids), len(ids[0]), len(h[0][0]), len(Wd[0])
+    y = [[0.0] * H for _ in range(T)]
+    for t in range(T):
+        for j in range(k):
+            e = ids[t][j]
+            for c in range(H):
+                y[t][c] += w[t][j] * sum(h[t][j][f] * Wd[e][c][f] for f in range(F))
+    return np.array(y)
+
+
+def _ffn_inputs(p):
+    return (_f64(p["x"]), _f64(p["Wg"]), _f64(p["Wu"]), _f64(p["Wd"]),
+            p["expert_ids"].numpy(), p["topk_weights"].numpy().astype(np.float64))
+
+
+def test_ffn_bruteforce_tiny():
+    p = workloads.ffn_problem(T=5, H=8, F=6, E=3, k=2, seed=3, routing="random")
+    x, Wg, Wu, Wd, ids, w = _ffn_inputs(p)
+    y, h = O.moe_ffn_forward(x, Wg, Wu, Wd, ids, w)
+    _, hpre = O.moe_ffn_forward(x, Wg, Wu, Wd, ids, w, round_h=False)
+    ref_pre = _brute_ffn_pre(x.tolist(), Wg.tolist(), Wu.tolist(), ids.tolist())
+    np.testing.assert_allclose(hpre, ref_pre, rtol=1e-12, atol=1e-14)
+    # h is the float32 value rounded to bfloat16 (torch's own cast here)
+    cast = torch.from_numpy(ref_pre.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(h, cast)
+    np.testing.assert_allclose(y, _brute_ffn_down(h.tolist(), Wd.tolist(), ids.tolist(), w.tolist()),
+                               rtol=1e-12, atol=1e-14)
+
+
+def test_silu_values():
+    assert O.silu(0.0) == 0.0
+    assert O.silu(1.0) == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), rel=1e-15)
+    assert O.silu(-1.0) == pytest.approx(-1.0 / (1.0 + math.e), rel=1e-15)
+    assert O.silu(60.0) == 60.0                       # sigmoid(60) rounds to 1
+    assert abs(O.silu(-60.0)) < 1e-24 and O.silu(-800.0) == 0.0   # exp overflows to inf
+
+
+def test_ffn_closed_forms():
+    p = workloads.ffn_problem(T=6, H=8, F=16, E=4, k=2, seed=5)
+    x, Wg, Wu, Wd, ids, w = _ffn_inputs(p)
+    y, h = O.moe_ffn_forward(x, Wg, np.zeros_like(Wu), Wd, ids, w)   # up = 0
+    assert not np.any(h) and not np.any(y)
+    y, h = O.moe_ffn_forward(x, np.zeros_like(Wg), Wu, Wd, ids, w)   # silu(0) = 0
+    assert not np.any(h) and not np.any(y)
+    # k = 1: the down projection is the pinned plain MoE forward of h
+    q = workloads.ffn_problem(T=7, H=8, F=16, E=3, k=1, seed=6)
+    x, Wg, Wu, Wd, ids, w = _ffn_inputs(q)
+    y, h = O.moe_ffn_forward(x, Wg, Wu, Wd, ids, w)
+    np.testing.assert_allclose(y, O.moe_forward(h[:, 0], Wd, ids, w), rtol=1e-13, atol=1e-15)
+    # token restriction matches the full result
+    yr, hr = O.moe_ffn_forward(x, Wg, Wu, Wd, ids, w, tokens=[4, 1])
+    np.testing.assert_array_equal(yr, y[[4, 1]])
+    np.testing.assert_array_equal(hr, h[[4, 1]])
+
+
 def test_planted_mistakes_are_caught():
     """Copies of oracle steps with one plausible mistake each fail a pin."""
     rng = np.random.default_rng(0)
@@ -516,6 +589,25 @@ def test_planted_mistakes_are_caught():
     for mutation in ("dx_transposed", "dx_unweighted", "dtopk_sign", "dw_wrong_token"):
         got = backward_with(mutation)
         assert not all(np.allclose(g, f, rtol=1e-9, atol=1e-11) for g, f in zip(got, fd)), mutation
+
+    f = workloads.ffn_problem(T=4, H=6, F=5, E=3, k=2, seed=9, routing="random")
+    fx, fg, fu, fd_, fi, fw = _ffn_inputs(f)
+    ref_pre = _brute_ffn_pre(fx.tolist(), fg.tolist(), fu.tolist(), fi.tolist())
+
+    def ffn_pre_with(mutation):              # the oracle's gated activation with one planted change
+        out = np.zeros((fi.shape[0], fi.shape[1], fg.shape[1]))
+        for j in range(fi.shape[1]):
+            for e in range(fg.shape[0]):
+                t = np.nonzero(fi[:, j] == e)[0]
+                g, u = fx[t] @ fg[e].T, fx[t] @ fu[e].T
+                if mutation == "gate_up_swapped":
+                    g, u = u, g
+                act = 1.0 / (1.0 + np.exp(-g)) if mutation == "sigmoid_not_silu" else O.silu(g)
+                out[t, j] = act * u
+        return out
+    np.testing.assert_allclose(ffn_pre_with(None), ref_pre, rtol=1e-12, atol=1e-14)
+    for mutation in ("gate_up_swapped", "sigmoid_not_silu"):
+        assert not np.allclose(ffn_pre_with(mutation), ref_pre, rtol=1e-6), mutation
 
     sched = O.tile_schedule([5, 0, 3], 48, 2, 16)
     row_major = []

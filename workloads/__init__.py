@@ -31,12 +31,14 @@ __all__ = [
     "bare_grouped",
     "moe_problem",
     "decode_problem",
+    "ffn_problem",
     "BARE_E4",
     "FWD_TOP2",
     "FWD_SKEW",
     "BWD_TOP2",
     "DECODE",
     "BWD_SMALL",
+    "FFN_TOP2",
 ]
 
 
@@ -148,6 +150,43 @@ def moe_problem(T: int, K: int, N: int, E: int, k: int, seed: int = 0,
     return out
 
 
+def ffn_problem(T: int, H: int, F: int, E: int, k: int, seed: int = 0,
+                routing: str = "uniform", zipf_s: float = 1.2,
+                weights: str = "uniform") -> dict:
+    """One gated expert-FFN problem ("Grouped GEMM for MoE, in depth",
+    §Choosing an implementation: gate and up projections, then the down
+    projection).
+
+    x[T,H] bf16 ~N(0,1); Wg, Wu [E,F,H] bf16 ~N(0,1/H); Wd [E,H,F] bf16
+    ~N(0,1/F); expert_ids[T,k] int32 and topk_weights[T,k] fp32 drawn as in
+    ``moe_problem`` (same ``routing`` and ``weights`` choices).
+    """
+    rng = np.random.default_rng(seed)
+    x = _normal(rng, (T, H))
+    Wg = _normal(rng, (E, F, H), std=1.0 / np.sqrt(H))
+    Wu = _normal(rng, (E, F, H), std=1.0 / np.sqrt(H))
+    Wd = _normal(rng, (E, H, F), std=1.0 / np.sqrt(F))
+    if routing == "uniform":
+        ids_ = _uniform_distinct_ids(rng, T, E, k)
+    elif routing == "zipf":
+        ids_ = _zipf_ids(rng, T, E, k, zipf_s)
+    elif routing == "random":
+        ids_ = rng.integers(0, E, size=(T, k), dtype=np.int32)
+    else:
+        raise ValueError(routing)
+    if weights == "uniform":
+        w = rng.random((T, k), dtype=np.float32)
+    elif weights == "softmax":
+        w = _softmax_weights(rng, T, k)
+    else:
+        raise ValueError(weights)
+    return {
+        "x": to_bf16(x), "Wg": to_bf16(Wg), "Wu": to_bf16(Wu), "Wd": to_bf16(Wd),
+        "expert_ids": torch.from_numpy(ids_), "topk_weights": torch.from_numpy(w),
+        "T": T, "H": H, "F": F, "E": E, "k": k,
+    }
+
+
 def decode_problem(E: int = 128, M_max: int = 64, K: int = 7168, N: int = 2048,
                    lam: float = 8.0, seed: int = 0, nan_masked: bool = True) -> dict:
     """Masked decode layout: x[E, M_max, K] bf16, W[E, N, K] bf16, masked_m[E].
@@ -184,3 +223,5 @@ DECODE = dict(E=128, M_max=64, K=7168, N=2048, lam=8.0, seed=0)
 # the 1/64-scale copy of the backward workload used for finite differences
 BWD_SMALL = dict(T=64, K=32, N=32, E=8, k=2, seed=0, routing="uniform", weights="pow2",
                  with_dy=True)
+# gated expert FFN, top-2: hidden 2048, FFN width 2048 (gate + up = 4096 columns)
+FFN_TOP2 = dict(T=4096, H=2048, F=2048, E=8, k=2, seed=0, routing="uniform", weights="uniform")
