@@ -416,6 +416,42 @@ def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
         "useful_row_fraction": round(float(counts.sum()) / (bm * sum(-(-int(m) // bm) for m in counts)), 4),
         "tiles": tiles, "count_min": int(counts.min()), "count_max": int(counts.max())}
     del args_, y, r
+    # gated expert FFN forward (gate+up GEMM with the SiLU-gated epilogue,
+    # down GEMM with the scatter-combine), top-2, H = F = 2048
+    c = workloads.FFN_TOP2
+    p = workloads.ffn_problem(**c)
+    T, H, F, E, k = c["T"], c["H"], c["F"], c["E"], c["k"]
+    fargs = [p[n].to(dev) for n in ("x", "Wg", "Wu", "Wd", "expert_ids", "topk_weights")]
+    yf = torch.empty(T, H, device=dev)
+    hf = torch.empty(T * k, F, dtype=torch.bfloat16, device=dev)
+    rf = mgg.RoutingBuffers.empty(T, k, E, dev)
+    ev2 = Events(2)
+    h2 = ev2.handles()
+    for _ in range(3):
+        mgg.moe_ffn_forward(*fargs, out=yf, h=hf, routing=rf)
+    t_all, t_gu, t_dn = [], [], []
+    for _ in range(10):
+        flush.zero_()
+        lib.mgg_set_kernel_events(h2, 2)
+        s0.record()
+        mgg.moe_ffn_forward(*fargs, out=yf, h=hf, routing=rf)
+        s1.record()
+        lib.mgg_set_kernel_events(None, 0)
+        torch.cuda.synchronize()
+        t_all.append(s0.elapsed_time(s1))
+        t_gu.append(ev2.ms(0))
+        t_dn.append(ev2.ms(1))
+    S = T * k
+    fl_gu, fl_dn = 2.0 * S * H * 2 * F, 2.0 * S * F * H
+    res["ffn_forward"] = {
+        "workload": "gated expert FFN forward (SiLU gating), top-2: T=4096, H=2048, F=2048, E=8, k=2, "
+                    "uniform distinct routing; seed 0",
+        "ms": round(statistics.mean(t_all), 4),
+        "tflops": round((fl_gu + fl_dn) / (statistics.mean(t_all) * 1e-3) / 1e12, 1),
+        "gate_up_gemm_tflops": round(fl_gu / (statistics.mean(t_gu) * 1e-3) / 1e12, 1),
+        "down_gemm_tflops": round(fl_dn / (statistics.mean(t_dn) * 1e-3) / 1e12, 1),
+        "useful_gflop": round((fl_gu + fl_dn) / 1e9, 3)}
+    del fargs, yf, hf, rf
     # masked decode under CUDA-graph replay (inputs 3.8 GB >> L2)
     c = workloads.DECODE
     E, M, K, N = c["E"], c["M_max"], c["K"], c["N"]

@@ -70,7 +70,8 @@ typedef enum {
   MGG_OP_FORWARD = 1,
   MGG_OP_BACKWARD = 2,
   MGG_OP_GROUPED_GEMM = 3,
-  MGG_OP_MASKED = 4
+  MGG_OP_MASKED = 4,
+  MGG_OP_FFN_FORWARD = 5
 } mgg_op;
 
 /* Bits the kernels OR into *dev_status. */
@@ -127,6 +128,7 @@ mgg_status mgg_tile_config(mgg_op op, mgg_dtype dtype, int* BM, int* BN, int* BK
  *   MGG_OP_BACKWARD              : T, k, E, N, K, dtype
  *   MGG_OP_GROUPED_GEMM          : E
  *   MGG_OP_MASKED                : 0 (no workspace)
+ *   MGG_OP_FFN_FORWARD           : T, k, E (N = H, K = F unused)
  */
 size_t mgg_workspace_bytes(mgg_op op, int T, int k, int E, int N, int K, mgg_dtype dtype);
 
@@ -255,6 +257,38 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
                             const mgg_routing* routing, int T, int K, int N, int E, int k,
                             mgg_dtype dtype, float* dx, float* dW, float* dtopk,
                             int32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Gated expert FFN forward, one MoE layer ("Grouped GEMM for MoE, in depth",
+ * §Choosing an implementation: the gate and up projections as one grouped
+ * GEMM with N doubled and the activation in its epilogue, then the down
+ * projection).  Per assignment a = (t, j), e = expert_ids[t, j]:
+ *   h_a  = bf16(silu(x[t] Wg_e^T) * (x[t] Wu_e^T))         [F]
+ *   y[t] = sum_j topk_weights[t, j] * h_a Wd_e^T            [H]
+ * with silu(v) = v / (1 + exp(-v)) (the page names no activation; SiLU
+ * gating is the reading taken).  Routing as mgg_route.  The gate/up GEMM
+ * gathers x rows on load (each of its 256-column tiles holds the gate and the
+ * up projection of the same 128 features); the down GEMM reads h in
+ * expert-sorted row order by TMA and scatters the rows, scaled by their
+ * routing weight and top-k combined, into y.
+ *   x       [T, H] bf16;  Wg, Wu [E, F, H] bf16;  Wd [E, H, F] bf16 (like
+ *           nn.Linear weights)
+ *   y       [T, H] f32, zeroed by the call, then accumulated atomically
+ *   h       [T*k, F] bf16, written: h[r] is the gated activation of sorted
+ *           row r, i.e. of assignment routing->row_assign[r] (the operand a
+ *           backward pass needs)
+ *   routing filled as by mgg_route with N = H (its tile_start counts the
+ *           down GEMM's tiles)
+ * bf16 only (MGG_ERR_DTYPE otherwise); H % 8 == 0 and F % 8 == 0
+ * (MGG_ERR_ALIGNMENT); 16-byte aligned pointers.  ws:
+ * mgg_workspace_bytes(MGG_OP_FFN_FORWARD, T, k, E, ...).  Other errors as
+ * for mgg_moe_forward.
+ */
+mgg_status mgg_moe_ffn_forward(const void* x, const void* Wg, const void* Wu, const void* Wd,
+                               const int32_t* expert_ids, const float* topk_weights, int T,
+                               int H, int F, int E, int k, mgg_dtype dtype, float* y, void* h,
+                               const mgg_routing* routing, int32_t* dev_status, void* ws,
+                               size_t ws_bytes, void* stream);
 
 /*
  * Debug export of the device tile schedule: for every tile index tau of the

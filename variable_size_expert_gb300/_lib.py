@@ -32,6 +32,7 @@ MGG_OP_FORWARD = 1
 MGG_OP_BACKWARD = 2
 MGG_OP_GROUPED_GEMM = 3
 MGG_OP_MASKED = 4
+MGG_OP_FFN_FORWARD = 5
 # device status bits
 MGG_DEV_BAD_EXPERT_ID = 0x1
 MGG_DEV_BAD_OFFSETS = 0x2
@@ -43,7 +44,7 @@ MGG_NOALLOC_SCRATCH_BYTES = 1 << 20
 EXPORTS = (
     "mgg_status_string", "mgg_tile_config", "mgg_workspace_bytes", "mgg_route",
     "mgg_grouped_gemm", "mgg_moe_forward", "mgg_moe_backward", "mgg_debug_tile_schedule",
-    "mgg_set_kernel_events", "mgg_route_noalloc",
+    "mgg_set_kernel_events", "mgg_route_noalloc", "mgg_moe_ffn_forward",
 )
 
 
@@ -75,6 +76,8 @@ _SIGS = {
     "mgg_debug_tile_schedule": (_I, [_RP, _I, _I, _I, _I, _P, _P]),
     "mgg_set_kernel_events": (_I, [ctypes.POINTER(_P), _I]),
     "mgg_route_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _RP, _P, _P]),
+    "mgg_moe_ffn_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _RP, _P,
+                                 _P, _SZ, _P]),
 }
 
 _lib = None

@@ -275,6 +275,9 @@ size_t mgg_workspace_bytes(mgg_op op, int T, int k, int E, int N, int K, mgg_dty
       return 2 * round256((E + 1) * sizeof(int32_t));
     case MGG_OP_MASKED:
       return 0;
+    case MGG_OP_FFN_FORWARD:
+      if (T < 1 || k < 1 || E < 1 || E > kMaxExperts) return 0;
+      return route_ws_bytes(T, k, E) + 2 * round256((E + 1) * sizeof(int32_t));
   }
   return 0;
 }
@@ -516,6 +519,82 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   CUtensorMap tm_dw;
   if (!tmap_dw_store(&tm_dw, dW, E, N, K)) return MGG_ERR_CUDA;
   return from_cuda(timed(1, st, [&] { return launch_dw_pair(tm_dyw, tm_dw, q, st); }));
+}
+
+mgg_status mgg_moe_ffn_forward(const void* x, const void* Wg, const void* Wu, const void* Wd,
+                               const int32_t* expert_ids, const float* topk_weights, int T,
+                               int H, int F, int E, int k, mgg_dtype dtype, float* y, void* h,
+                               const mgg_routing* routing, int32_t* dev_status, void* ws,
+                               size_t ws_bytes, void* stream) {
+  if (!x || !Wg || !Wu || !Wd || !expert_ids || !topk_weights || !y || !h ||
+      !routing_ok(routing) || !dev_status || !ws)
+    return MGG_ERR_INVALID_ARG;
+  if (dtype != MGG_BF16) return MGG_ERR_DTYPE;
+  mgg_status s = check_moe_sizes(T, H, H, E, k, dtype);
+  if (s != MGG_OK) return s;
+  if (F < 1) return MGG_ERR_INVALID_ARG;
+  if (F % 8 != 0) return MGG_ERR_ALIGNMENT;
+  if (!aligned(x, 16) || !aligned(Wg, 16) || !aligned(Wu, 16) || !aligned(Wd, 16) ||
+      !aligned(y, 16) || !aligned(h, 16))
+    return MGG_ERR_ALIGNMENT;
+  if (ws_bytes < mgg_workspace_bytes(MGG_OP_FFN_FORWARD, T, k, E, H, F, dtype) || !aligned(ws, 256))
+    return MGG_ERR_WORKSPACE;
+  s = check_arch();
+  if (s != MGG_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t off_gu = route_ws_bytes(T, k, E);
+  int32_t* tile_start_gu = at<int32_t>(ws, off_gu);
+  int32_t* scratch = at<int32_t>(ws, off_gu + round256((E + 1) * sizeof(int32_t)));
+  // routing with the down GEMM's tiles (256 x 256 over H), y zeroed
+  cudaError_t e = launch_route(expert_ids, topk_weights, T, k, E, kPairBM, cdiv(H, kPairBN),
+                               routing->counts, routing->end_offs, routing->start,
+                               routing->tile_start, routing->row_assign, routing->row_token,
+                               routing->row_weight, dev_status, ws, st, y,
+                               static_cast<size_t>(T) * H);
+  if (e != cudaSuccess) return MGG_ERR_CUDA;
+  // the gate/up GEMM's tiles: 256 rows x 128 features (gate and up side by side)
+  if (launch_bwd_scan(routing->counts, E, kPairBM, cdiv(F, kPairBN / 2), kDwPad, tile_start_gu,
+                      scratch, st) != cudaSuccess)
+    return MGG_ERR_CUDA;
+  RowsParams p{};
+  p.A = x;
+  p.lda = H;
+  p.Kc = H;
+  p.row_token = routing->row_token;
+  p.row_weight = routing->row_weight;
+  p.tile_start = tile_start_gu;
+  p.start = routing->start;
+  p.E = E;
+  p.Nout = F;
+  p.hout = h;
+  p.ldh = F;
+  p.dev_status = dev_status;
+  p.wait_limit = wait_limit();
+  CUtensorMap tg, tu;
+  if (!tmap_weights(&tg, Wg, E, F, H, kBK, kPairBN / 2) ||
+      !tmap_weights(&tu, Wu, E, F, H, kBK, kPairBN / 2))
+    return MGG_ERR_CUDA;
+  if (timed(0, st, [&] { return launch_rows_pair(kModeGateUp, false, tu, tg, p, st); }) !=
+      cudaSuccess)
+    return MGG_ERR_CUDA;
+  // down projection: h rows in sorted order by TMA, scatter-combine into y
+  RowsParams q{};
+  q.Kc = F;
+  q.lda = F;
+  q.row_token = routing->row_token;
+  q.row_weight = routing->row_weight;
+  q.tile_start = routing->tile_start;
+  q.start = routing->start;
+  q.E = E;
+  q.Nout = H;
+  q.out = y;
+  q.ldo = H;
+  q.dev_status = dev_status;
+  q.wait_limit = wait_limit();
+  CUtensorMap th, td;
+  if (!tmap_rows(&th, h, T * k, F, kPairBM / 2) || !tmap_weights(&td, Wd, E, H, F, kBK, kPairBN / 2))
+    return MGG_ERR_CUDA;
+  return from_cuda(timed(1, st, [&] { return launch_rows_pair(kModeScatter, false, th, td, q, st); }));
 }
 
 mgg_status mgg_debug_tile_schedule(const mgg_routing* routing, int E, int N, mgg_dtype dtype,

@@ -160,12 +160,24 @@ __device__ __forceinline__ void pair_teardown(uint32_t tmem_base, int warp) {
   }
 }
 
+// silu(v) = v / (1 + exp(-v)) with the fast exponential and divide
+// intrinsics (h is rounded to bf16 next).  The exponent is clamped at 80 so
+// the denominator stays below 2^126, the fast divide's range; below v = -80
+// the true value is under 1e-32 in magnitude either way.
+__device__ __forceinline__ float silu_fast(float v) {
+  return __fdividef(v, 1.f + __expf(fminf(-v, 80.f)));
+}
+
 // ====================================================================== rows
 template <int MODE, bool B_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     rows_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b, const RowsParams p) {
-  constexpr bool GATHER = MODE != kModeBare;
+  // A rows gathered through row_token (else loaded in sorted order by TMA);
+  // output added into token rows (else stored in sorted row order)
+  constexpr bool GATHER = MODE == kModeFused || MODE == kModeFusedDtopk || MODE == kModeGateUp;
+  constexpr bool SCATTER = MODE == kModeFused || MODE == kModeFusedDtopk || MODE == kModeScatter;
+  constexpr bool GATEUP = MODE == kModeGateUp;
   extern __shared__ uint8_t smem_raw[];
   constexpr int STAGES = kRowsStages;
   const PairSmem m = carve<STAGES, kRowsEpi>(smem_raw);
@@ -177,7 +189,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const int npairs = gridDim.x >> 1;
 
   if (warp == 5 && lane == 0) {
-    if (!GATHER) tma_prefetch_desc(&tmap_a);
+    if (!GATHER || GATEUP) tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
   }
   const uint32_t tmem_base = pair_setup<STAGES>(m, GATHER ? 2 : 1, warp);
@@ -285,7 +297,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                             t.row0 + static_cast<int>(rank) * CBM);
           const uint32_t dB = m.sB + s * B_STAGE;
           const int n0 = t.nb * PBN + static_cast<int>(rank) * CBN;
-          if (SPLIT && w.nhalves == 2) {
+          if (GATEUP) {
+            // gate rows into the even CTA, up rows into the odd one: MMA
+            // columns 0..127 are the gate, 128..255 the up projection of the
+            // same 128 features
+            tma_load_3d_cg2(dB, rank == 0 ? &tmap_b : &tmap_a, fb, kb * BK, t.nb * (PBN / 2), t.e);
+          } else if (SPLIT && w.nhalves == 2) {
             // a half's 64 B rows are the first 64 of a 128-row box at a
             // shifted row (the other 64 are loaded and not read)
             const int nh = t.nb * PBN + w.half * (PBN / 2) + static_cast<int>(rank) * (CBN / 2);
@@ -382,7 +399,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int r_own = ro + lane;
         int o_own = t.row0 + r_own;
         float w_own = 1.f;
-        if (MODE != kModeBare && r_own < t.rows) {
+        if (SCATTER && r_own < t.rows) {
           o_own = __ldg(p.row_token + t.row0 + r_own);
           w_own = __ldg(p.row_weight + t.row0 + r_own);
         }
@@ -414,6 +431,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (!__all_sync(0xffffffffu, wait_bar(m.acc_full + 8 * acc, use & 1, wc))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * PBN;
+      if (GATEUP) {
+        // h = bf16(silu(gate) * up) for the warp's 32 rows and the tile's 128
+        // features: accumulator columns c (gate) and 128 + c (up).  Each
+        // 64-feature half (128 bytes of an h row per lane) goes through the
+        // staging buffer like the f32 blocks, so every store instruction
+        // writes four rows x 128 contiguous bytes of h.
+        const int f0 = t.nb * (PBN / 2);
+#pragma unroll 1
+        for (int cp = 0; cp < 2; ++cp) {
+#pragma unroll 1
+          for (int hb = 0; hb < 2; ++hb) {
+            const int c0 = cp * 64 + hb * 32;
+            float g[32], u[32];
+            tmem_ld32(taddr + c0, g);
+            tmem_ld32(taddr + PBN / 2 + c0, u);
+            tmem_ld_wait();
+            if (cp == 1 && hb == 1) {  // accumulator fully read
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
+            }
+            uint32_t hv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              hv[i] = pack_bf16x2_rn(silu_fast(g[2 * i]) * u[2 * i],
+                                     silu_fast(g[2 * i + 1]) * u[2 * i + 1]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(stg + lane * 128 + (((hb * 4 + q) ^ (lane & 7)) << 4),
+                           __uint_as_float(hv[4 * q]), __uint_as_float(hv[4 * q + 1]),
+                           __uint_as_float(hv[4 * q + 2]), __uint_as_float(hv[4 * q + 3]));
+          }
+          __syncwarp();
+          const int col = f0 + cp * 64 + 8 * kq;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int rl = 4 * j + rq;
+            const float4 v = ld_shared_v4(stg + rl * 128 + ((kq ^ (rl & 7)) << 4));
+            if (ro + rl < t.rows && col < p.Nout)
+              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.hout) +
+                                        static_cast<long long>(t.row0 + ro + rl) * p.ldh + col) =
+                  make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                             __float_as_uint(v.w));
+          }
+          __syncwarp();
+        }
+        ++tcount;
+        continue;
+      }
       float dot[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) dot[j] = 0.f;
@@ -443,7 +509,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const float4 u = ld_shared_v4(stg + rl * 128 + ((kq ^ (rl & 7)) << 4));
           if (ro + rl < t.rows && col < p.Nout) {
             float* o = p.out + static_cast<long long>(orow[j]) * p.ldo + col;
-            if (MODE == kModeBare) {
+            if (!SCATTER) {
               *reinterpret_cast<float4*>(o) = u;
             } else {
               atomicAdd(reinterpret_cast<float4*>(o),
@@ -829,6 +895,9 @@ cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_
   if (!b_mn_major) {
     if (mode == kModeBare) return launch_rows_pair_t<kModeBare, false>(tmap_a, tmap_b, p, st);
     if (mode == kModeFused) return launch_rows_pair_t<kModeFused, false>(tmap_a, tmap_b, p, st);
+    if (mode == kModeGateUp) return launch_rows_pair_t<kModeGateUp, false>(tmap_a, tmap_b, p, st);
+    if (mode == kModeScatter)
+      return launch_rows_pair_t<kModeScatter, false>(tmap_a, tmap_b, p, st);
   } else {
     if (mode == kModeFusedDtopk)
       return launch_rows_pair_t<kModeFusedDtopk, true>(tmap_a, tmap_b, p, st);

@@ -24,7 +24,17 @@ constexpr int kMaxExperts = 1024;
 // Default pipeline wait limit in SM clock cycles (about a second).
 constexpr long long kDefaultWaitLimit = 2000000000LL;
 
-enum RowsMode { kModeBare = 0, kModeFused = 1, kModeFusedDtopk = 2 };
+// Row GEMM modes: A gathered through row_token (fused, fused + dtopk, gate/up)
+// or loaded in sorted order (bare, scatter); output stored in sorted order
+// (bare), weighted and added into token rows (fused, fused + dtopk,
+// scatter), or gated into bf16 h (gate/up).
+enum RowsMode {
+  kModeBare = 0,
+  kModeFused = 1,
+  kModeFusedDtopk = 2,
+  kModeGateUp = 3,
+  kModeScatter = 4
+};
 
 // One launch of the row-gathering grouped GEMM (forward, bare, dX).
 struct RowsParams {
@@ -44,6 +54,8 @@ struct RowsParams {
   int ldx;
   float* dtopk;                // dtopk: [S] indexed by assignment
   int b_merged;                // MN-major B: tmap_b is the 4-D chunked view, one box per stage
+  void* hout;                  // gate/up: h [S, ldh] bf16, sorted rows
+  int ldh;
   int32_t* dev_status;
   long long wait_limit;
 };

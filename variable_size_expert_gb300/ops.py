@@ -22,6 +22,7 @@ from . import _lib as L
 __all__ = [
     "RoutingBuffers", "route", "moe_forward", "moe_backward", "moe", "grouped_gemm",
     "grouped_gemm_masked", "debug_tile_schedule", "tile_config", "workspace_bytes",
+    "moe_ffn_forward",
     "new_status", "read_status",
 ]
 
@@ -153,6 +154,38 @@ def moe_forward(x: torch.Tensor, W: torch.Tensor, expert_ids: torch.Tensor,
                                 _ptr(y), ctypes.byref(rs), _ptr(st), _ptr(ws), ws.numel(),
                                 _stream()), "mgg_moe_forward")
     return y, r
+
+
+def moe_ffn_forward(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor,
+                    expert_ids: torch.Tensor, topk_weights: torch.Tensor,
+                    status: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                    h: torch.Tensor | None = None, routing: RoutingBuffers | None = None,
+                    workspace: torch.Tensor | None = None):
+    """Gated expert FFN forward (bf16).  Returns (y [T, H] float32, h [T*k, F]
+    bf16 in expert-sorted row order, routing)."""
+    lib = L.load()
+    if x.dtype != torch.bfloat16 or not (Wg.dtype == Wu.dtype == Wd.dtype == torch.bfloat16):
+        raise TypeError("the gated FFN path takes bfloat16 x and weights")
+    T, H = x.shape
+    E, F, H2 = Wg.shape
+    if H2 != H or tuple(Wu.shape) != (E, F, H) or tuple(Wd.shape) != (E, H, F):
+        raise ValueError("expected Wg, Wu [E, F, H] and Wd [E, H, F] with the H of x")
+    ids = _ids_i32(expert_ids).contiguous()
+    w = topk_weights.detach().contiguous().float()
+    k = ids.shape[1]
+    dev = x.device
+    y = out if out is not None else torch.empty(T, H, dtype=torch.float32, device=dev)
+    hb = h if h is not None else torch.empty(T * k, F, dtype=torch.bfloat16, device=dev)
+    r = routing or RoutingBuffers.empty(T, k, E, dev)
+    st = status if status is not None else new_status(dev)
+    nbytes = lib.mgg_workspace_bytes(L.MGG_OP_FFN_FORWARD, T, k, E, H, F, L.MGG_BF16)
+    ws = workspace if workspace is not None and workspace.numel() >= nbytes else _workspace(nbytes, dev)
+    rs = r.struct()
+    L.check(lib.mgg_moe_ffn_forward(_ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(ids), _ptr(w), T,
+                                    H, F, E, k, L.MGG_BF16, _ptr(y), _ptr(hb), ctypes.byref(rs),
+                                    _ptr(st), _ptr(ws), ws.numel(), _stream()),
+            "mgg_moe_ffn_forward")
+    return y, hb, r
 
 
 def moe_backward(dy: torch.Tensor, x: torch.Tensor, W: torch.Tensor, routing: RoutingBuffers,
