@@ -200,15 +200,15 @@ bool encode_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* d
   return r == CUDA_SUCCESS;
 }
 
-// f32 [E][N][K] (dW) as a 3-D map for TMA tile stores, box {128, 32, 1}, no
-// swizzle: the staged block is row-major like the tensor.
+// f32 [E][N][K] (dW) as a 3-D map for TMA tile stores, box {32, 32, 1} (one
+// warp's block), no swizzle: the staged block is row-major like the tensor.
 bool tmap_dw_store(CUtensorMap* map, float* dW, int E, int N, int K) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = tmap_encoder();
   if (!fn) return false;
   cuuint64_t d[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
                      static_cast<cuuint64_t>(E)};
   cuuint64_t st[2] = {static_cast<cuuint64_t>(K) * 4, static_cast<cuuint64_t>(N) * K * 4};
-  cuuint32_t b[3] = {128, 32, 1};
+  cuuint32_t b[3] = {32, 32, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dW, d, st, b, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

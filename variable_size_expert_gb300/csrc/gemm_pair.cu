@@ -61,8 +61,8 @@ constexpr int NUM_THREADS = 320;
 constexpr int TMEM_COLS = 2 * PBN;
 constexpr int EPI_WARP = 32 * 32 * 4;  // one warp's 32 x 32 f32 staging block
 constexpr int kRowsEpi = 4 * EPI_WARP;
-constexpr int DW_EPI_BUF = 32 * CBM * 4;  // one 32 (n) x 128 (k) f32 block
-constexpr int kDwEpi = 2 * DW_EPI_BUF;
+constexpr int DW_EPI_BUF = 32 * 32 * 4;  // one warp's 32 (n) x 32 (k) f32 block
+constexpr int kDwEpi = 4 * 2 * DW_EPI_BUF;  // double-buffered per epilogue warp
 constexpr int kBarBytes = 256;
 template <int STAGES, int EPI_BYTES>
 constexpr size_t smem_bytes() {
@@ -591,7 +591,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const int npairs = gridDim.x >> 1;
 
   if (warp == 5 && lane == 0) tma_prefetch_desc(&tmap_dyw);
-  if (threadIdx.x == 0) tma_prefetch_desc(&tmap_dw);
+  if (warp < 4 && lane == 0) tma_prefetch_desc(&tmap_dw);
   const uint32_t tmem_base = pair_setup<STAGES>(m, 2, warp);
   const uint32_t full_l = mapa_shared(m.full, 0);
   const uint32_t acc_empty_l = mapa_shared(m.acc_empty, 0);
@@ -780,18 +780,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------ epilogue (128 threads per CTA)
     // Lane i of warp w holds dW column k = k0 + 32 w + i (TMEM lane), 32
-    // output rows n per block.  The four warps write each 32 (n) x 128 (k)
-    // block into one of two staging buffers, row-major like dW itself, and
-    // thread 0 stores it with one TMA tile store (clipped at N and K), so
-    // the output leaves without load/store-unit traffic.  Named barrier 1
-    // (these 128 threads) orders the buffer hand-offs; the tile loop's one
-    // wait is taken as a single decision of all four warps.
-    const bool issuer = threadIdx.x == 0;
+    // output rows n per block.  Each warp writes its 32 (n) x 32 (k) block
+    // into one of its two staging buffers, row-major like dW itself, and its
+    // lane 0 stores it with one TMA tile store (clipped at N and K), so the
+    // output leaves without load/store-unit traffic and the warps never wait
+    // for one another.
+    const uint32_t stg0 = m.sEpi + warp * 2 * DW_EPI_BUF;
     int tcount = 0, nst = 0;
     for (int tau = pair; tau < total; tau += npairs) {
       const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts);
-      const int k0 = t.kbo * PBM + static_cast<int>(rank) * CBM;
-      const int kcol = k0 + warp * 32 + lane;
+      const int kw = t.kbo * PBM + static_cast<int>(rank) * CBM + warp * 32;  // warp's first k
+      const int kcol = kw + lane;
       const int n0 = t.nb * PBN;
       if (t.nkb == 0) {
         // expert with no rows: its gradient is exactly zero, and is written
@@ -802,7 +801,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       }
       const int acc = tcount & 1;
       const uint32_t use = tcount >> 1;
-      if (!bar_and(1, 128, wait_bar(m.acc_full + 8 * acc, use & 1, wc))) break;
+      if (!__all_sync(0xffffffffu, wait_bar(m.acc_full + 8 * acc, use & 1, wc))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * PBN;
       const int nch = std::min(PBN / 32, cdiv(p.N - n0, 32));
@@ -816,22 +815,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
         }
-        const uint32_t buf = m.sEpi + (nst & 1) * DW_EPI_BUF;
-        if (issuer) bulk_wait_read<1>();  // the store two blocks ago has read this buffer
-        bar_named(1, 128);
+        const uint32_t buf = stg0 + (nst & 1) * DW_EPI_BUF;
+        if (lane == 0) bulk_wait_read<1>();  // the store two blocks ago has read this buffer
+        __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) st_shared_f32(buf + i * (CBM * 4) + (warp * 32 + lane) * 4, v[i]);
+        for (int i = 0; i < 32; ++i) st_shared_f32(buf + i * 128 + lane * 4, v[i]);
         fence_proxy_async_smem();
-        bar_named(1, 128);
-        if (issuer && k0 < p.K) {  // (a block wholly past K is not stored)
-          tma_store_3d(&tmap_dw, buf, k0, n0 + cc * 32, t.e);
+        __syncwarp();
+        if (lane == 0 && kw < p.K) {  // (a block wholly past K is not stored)
+          tma_store_3d(&tmap_dw, buf, kw, n0 + cc * 32, t.e);
           bulk_commit();
         }
         ++nst;
       }
       ++tcount;
     }
-    if (issuer) bulk_wait<0>();
+    if (lane == 0) bulk_wait<0>();
   }
 
   pair_teardown(tmem_base, warp);

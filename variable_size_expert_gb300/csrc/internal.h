@@ -118,7 +118,7 @@ cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* star
 // gemm_pair.cu (tcgen05, cta_group::2)
 cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_a,
                              const CUtensorMap& tmap_b, const RowsParams& p, cudaStream_t st);
-// tmap_dw: dW [E][N][K] f32 as a 3-D map, box {128, 32, 1}, no swizzle.
+// tmap_dw: dW [E][N][K] f32 as a 3-D map, box {32, 32, 1}, no swizzle.
 cudaError_t launch_dw_pair(const CUtensorMap& tmap_dyw, const CUtensorMap& tmap_dw,
                            const DwParams& p, cudaStream_t st);
 // gemm_masked.cu (tcgen05)
