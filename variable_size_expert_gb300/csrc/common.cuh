@@ -84,6 +84,34 @@ __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, lo
   return true;
 }
 
+// ---------------------------------------------------------------- PDL
+// Programmatic dependent launch.  A kernel launched with launch_pdl may be
+// scheduled while the previous kernel in the stream is still running (once
+// that kernel's blocks have all signalled pdl_trigger or exited); before it
+// touches memory the previous kernel may write, every thread calls pdl_wait,
+// which returns once the previous kernel has completed and its writes are
+// visible.  With no signalling predecessor both are no-ops in effect.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");

@@ -192,7 +192,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (!GATHER || GATEUP) tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
   }
+  pdl_trigger();
   const uint32_t tmem_base = pair_setup<STAGES>(m, GATHER ? 2 : 1, warp);
+  pdl_wait();  // the inputs may be the previous kernel's outputs
   const uint32_t full_l = mapa_shared(m.full, 0);           // leader's full[0]
   const uint32_t acc_empty_l = mapa_shared(m.acc_empty, 0);  // leader's acc_empty[0]
 
@@ -592,7 +594,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 5 && lane == 0) tma_prefetch_desc(&tmap_dyw);
   if (warp < 4 && lane == 0) tma_prefetch_desc(&tmap_dw);
+  pdl_trigger();
   const uint32_t tmem_base = pair_setup<STAGES>(m, 2, warp);
+  pdl_wait();  // the inputs may be the previous kernel's outputs
   const uint32_t full_l = mapa_shared(m.full, 0);
   const uint32_t acc_empty_l = mapa_shared(m.acc_empty, 0);
 
@@ -883,8 +887,7 @@ cudaError_t launch_rows_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
   constexpr size_t smem = smem_bytes<kRowsStages, kRowsEpi>();
   cudaError_t e = prepare(kern, smem, done);
   if (e != cudaSuccess) return e;
-  kern<<<pair_grid(kern, smem), NUM_THREADS, smem, st>>>(ta, tb, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(pair_grid(kern, smem)), dim3(NUM_THREADS), smem, st, ta, tb, p);
 }
 
 }  // namespace
@@ -910,8 +913,8 @@ cudaError_t launch_dw_pair(const CUtensorMap& tmap_dyw, const CUtensorMap& tmap_
   constexpr size_t smem = smem_bytes<kDwStages, kDwEpi>();
   cudaError_t e = prepare(dw_pair_kernel, smem, done);
   if (e != cudaSuccess) return e;
-  dw_pair_kernel<<<pair_grid(dw_pair_kernel, smem), NUM_THREADS, smem, st>>>(tmap_dyw, tmap_dw, p);
-  return cudaGetLastError();
+  return launch_pdl(dw_pair_kernel, dim3(pair_grid(dw_pair_kernel, smem)), dim3(NUM_THREADS), smem,
+                    st, tmap_dyw, tmap_dw, p);
 }
 
 }  // namespace mgg

@@ -156,6 +156,8 @@ __global__ void __launch_bounds__(1024)
                        int32_t* __restrict__ tile_start, int32_t* __restrict__ row_assign,
                        int32_t* __restrict__ row_token, float* __restrict__ row_weight,
                        int32_t* dev_status, float4* __restrict__ zero, long long nzero4) {
+  pdl_trigger();
+  pdl_wait();  // y, the routing buffers and ids may belong to the previous kernel
   if (blockIdx.x > 0) {
     const long long stride = static_cast<long long>(gridDim.x - 1) * blockDim.x;
     for (long long i = static_cast<long long>(blockIdx.x - 1) * blockDim.x + threadIdx.x;
@@ -267,6 +269,8 @@ __global__ void offsets_scan_kernel(const int32_t* __restrict__ offs, int is_siz
 __global__ void bwd_scan_kernel(const int32_t* __restrict__ counts, int E, int BM, int tiles_n,
                                 int pad, int32_t* __restrict__ tile_start_dx,
                                 int32_t* __restrict__ pstart) {
+  pdl_trigger();
+  pdl_wait();
   const int e = threadIdx.x;
   const int m = e < E ? counts[e] : 0;
   int total_tiles, total_pad;
@@ -312,6 +316,8 @@ __global__ void __launch_bounds__(kPrepThreads)
                     const int32_t* __restrict__ row_assign,
                     const float* __restrict__ row_weight, int E, uint4* __restrict__ dyw,
                     uint4* __restrict__ dy_b, float4* __restrict__ dx, float* __restrict__ dtopk) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int s_pstart[kMaxExperts + 1];
   __shared__ int s_start[kMaxExperts];
   __shared__ int s_count[kMaxExperts];
@@ -440,11 +446,10 @@ cudaError_t launch_route(const int32_t* ids, const float* w, int T, int k, int E
   const bool fuse_zero = zero && zero_floats % 4 == 0 && reinterpret_cast<uintptr_t>(zero) % 16 == 0;
   if (S <= kRouteSmallS && E <= kRouteSmallE) {
     const int blocks = 1 + (fuse_zero && zero_floats > 0 ? std::max(1, num_sms() - 1) : 0);
-    route_small_kernel<<<blocks, 1024, 0, st>>>(
-        ids, w, S, k, E, BM, tiles_n, counts, end_offs, start, tile_start, row_assign, row_token,
-        row_weight, dev_status, reinterpret_cast<float4*>(zero),
-        fuse_zero ? static_cast<long long>(zero_floats / 4) : 0);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(
+        route_small_kernel, dim3(blocks), dim3(1024), 0, st, ids, w, S, k, E, BM, tiles_n, counts,
+        end_offs, start, tile_start, row_assign, row_token, row_weight, dev_status,
+        reinterpret_cast<float4*>(zero), fuse_zero ? static_cast<long long>(zero_floats / 4) : 0);
     if (e == cudaSuccess && zero && !fuse_zero && zero_floats > 0)
       e = cudaMemsetAsync(zero, 0, zero_floats * sizeof(float), st);
     return e;
@@ -473,8 +478,8 @@ cudaError_t launch_offsets_scan(const int32_t* offs, bool is_sizes, int E, int r
 
 cudaError_t launch_bwd_scan(const int32_t* counts, int E, int BM, int tiles_n, int pad,
                             int32_t* tile_start_dx, int32_t* pstart, cudaStream_t st) {
-  bwd_scan_kernel<<<1, kScanThreads, 0, st>>>(counts, E, BM, tiles_n, pad, tile_start_dx, pstart);
-  return cudaGetLastError();
+  return launch_pdl(bwd_scan_kernel, dim3(1), dim3(kScanThreads), 0, st, counts, E, BM, tiles_n,
+                    pad, tile_start_dx, pstart);
 }
 
 cudaError_t launch_bwd_prep(const float* dy, int N, int K, int k, const int32_t* counts,
@@ -485,11 +490,10 @@ cudaError_t launch_bwd_prep(const float* dy, int N, int K, int k, const int32_t*
                             cudaStream_t st) {
   const int wpb = kPrepThreads / 32;
   const int blocks = std::max(1, std::min(cdiv(S_pad_max, wpb), num_sms() * (2048 / kPrepThreads)));
-  bwd_prep_kernel<<<blocks, kPrepThreads, 0, st>>>(
-      dy, N, K, k, counts, start, BM, tiles_n, pad, tile_start_dx, pstart, row_token, row_assign,
-      row_weight, E,
-      static_cast<uint4*>(dyw), static_cast<uint4*>(dy_b), reinterpret_cast<float4*>(dx), dtopk);
-  return cudaGetLastError();
+  return launch_pdl(bwd_prep_kernel, dim3(blocks), dim3(kPrepThreads), 0, st, dy, N, K, k, counts,
+                    start, BM, tiles_n, pad, tile_start_dx, pstart, row_token, row_assign,
+                    row_weight, E, static_cast<uint4*>(dyw), static_cast<uint4*>(dy_b),
+                    reinterpret_cast<float4*>(dx), dtopk);
 }
 
 cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* start, int E, int BM,
