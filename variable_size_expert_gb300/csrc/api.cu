@@ -124,7 +124,7 @@ bool tmap_rows(CUtensorMap* m, const void* base, int rows, int cols, int box_row
 }
 
 struct BwdLayout {
-  size_t off_tile_start_dx, off_pstart, off_dy_b, off_dyw, total;
+  size_t off_tile_start_dx, off_pstart, off_order, off_dy_b, off_dyw, total;
   int S_pad_max;
 };
 
@@ -137,6 +137,8 @@ BwdLayout bwd_layout(int T, int k, int E, int N, int K, mgg_dtype dt) {
   off += round256((E + 1) * sizeof(int32_t));
   L.off_pstart = off;
   off += round256((E + 1) * sizeof(int32_t));
+  L.off_order = off;
+  off += round256(E * sizeof(int32_t));
   L.S_pad_max = 0;
   if (dt == MGG_BF16) {
     L.off_dy_b = off;
@@ -480,13 +482,16 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
 
   void* dy_b = at<void>(ws, L.off_dy_b);
   void* dyw = at<void>(ws, L.off_dyw);
+  // expert visiting order of the dW GEMM (decreasing row count), for up to
+  // 256 experts; index order beyond
+  int32_t* order = E <= 256 ? at<int32_t>(ws, L.off_order) : nullptr;
   // one pass over dy: the backward schedules (dX tile prefix sums, padded
   // segment starts), the bf16 operands of both GEMMs, and dx, dtopk zeroed
   // for the dX epilogue's atomic adds
   if (launch_bwd_prep(dy, N, K, k, routing->counts, routing->start, BM, cdiv(K, BN), kDwPad,
                       tile_start_dx, pstart, routing->row_token, routing->row_assign,
-                      routing->row_weight, E, L.S_pad_max, dy_b, dyw, dx, dtopk,
-                      st) != cudaSuccess)
+                      routing->row_weight, E, L.S_pad_max, dy_b, dyw, dx, dtopk, st,
+                      order) != cudaSuccess)
     return MGG_ERR_CUDA;
   p.A = dy_b;
   // dX reads W_e transposed: per stage each CTA takes 64 contraction rows of
@@ -501,6 +506,7 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
 
   // dW's B operand, the scaled sorted dY [S_pad, N]: same choice over N.
   q.dyw = dyw;
+  q.expert_order = order;
   CUtensorMap tm_dyw;
   q.b_merged = 0;
   if (N % 64 == 0) {

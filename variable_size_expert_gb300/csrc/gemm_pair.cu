@@ -560,12 +560,18 @@ struct DwTile {
   int e, kbo, nb, m, nkb;
 };
 
+// Tile tau -> (expert, n block, k block): experts in the order given (the
+// backward prep ranks them by decreasing row count, so the static stride
+// hands out the longest contractions first and the last round holds the
+// shortest), n blocks, then k blocks fastest.
 __device__ __forceinline__ DwTile decode_dw(int tau, int tiles_k, int tiles_n,
-                                            const int32_t* __restrict__ counts) {
+                                            const int32_t* __restrict__ counts,
+                                            const int32_t* __restrict__ order) {
   DwTile t;
   const int per = tiles_k * tiles_n;
-  t.e = tau / per;
-  const int local = tau - t.e * per;
+  const int eo = tau / per;
+  t.e = order ? __ldg(order + eo) : eo;
+  const int local = tau - eo * per;
   t.nb = local / tiles_k;
   t.kbo = local - t.nb * tiles_k;
   t.m = __ldg(counts + t.e);
@@ -619,7 +625,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     };
     auto seek = [&](Cur& cu) {
       while (cu.tau < total) {
-        const DwTile t = decode_dw(cu.tau, tiles_k, tiles_n, p.counts);
+        const DwTile t = decode_dw(cu.tau, tiles_k, tiles_n, p.counts, p.expert_order);
         if (t.nkb > 0) {
           cu.nkb = t.nkb;
           cu.m = t.m;
@@ -703,7 +709,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       int it = 0;
       bool ok = true;
       for (int tau = pair; ok && tau < total; tau += npairs) {
-        const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts);
+        const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
         const int ps = __ldg(p.pstart + t.e);
         const int n0 = t.nb * PBN + static_cast<int>(rank) * CBN;
         for (int kb = 0; kb < t.nkb; ++kb) {
@@ -737,7 +743,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       int it = 0;
       bool ok = true;
       for (int tau = pair; ok && tau < total; tau += npairs) {
-        const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts);
+        const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
         for (int kb = 0; kb < t.nkb; ++kb, ++it)
           if (!relay_stage<STAGES>(m, full_l, it, wc)) {
             ok = false;
@@ -750,7 +756,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       int it = 0, tcount = 0;
       bool ok = true;
       for (int tau = pair; ok && tau < total; tau += npairs) {
-        const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts);
+        const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
         if (t.nkb == 0) continue;
         const int acc = tcount & 1;
         const uint32_t use = tcount >> 1;
@@ -792,7 +798,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const uint32_t stg0 = m.sEpi + warp * 2 * DW_EPI_BUF;
     int tcount = 0, nst = 0;
     for (int tau = pair; tau < total; tau += npairs) {
-      const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts);
+      const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
       const int kw = t.kbo * PBM + static_cast<int>(rank) * CBM + warp * 32;  // warp's first k
       const int kcol = kw + lane;
       const int n0 = t.nb * PBN;

@@ -74,6 +74,7 @@ struct DwParams {
   int E;
   float* dW;                   // [E, N, K]
   int b_merged;                // tmap_dyw is the 3-D chunked view, one box per stage
+  const int32_t* expert_order;  // [E] experts by decreasing row count (null: index order)
   int32_t* dev_status;
   long long wait_limit;
 };
@@ -111,7 +112,7 @@ cudaError_t launch_bwd_prep(const float* dy, int N, int K, int k, const int32_t*
                             int32_t* tile_start_dx, int32_t* pstart, const int32_t* row_token,
                             const int32_t* row_assign, const float* row_weight, int E,
                             int S_pad_max, void* dy_b, void* dyw, float* dx, float* dtopk,
-                            cudaStream_t st);
+                            cudaStream_t st, int32_t* expert_order = nullptr);
 cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* start, int E, int BM,
                                   int max_tiles, int32_t* out, cudaStream_t st);
 

@@ -315,7 +315,8 @@ __global__ void __launch_bounds__(kPrepThreads)
                     int32_t* __restrict__ pstart, const int32_t* __restrict__ row_token,
                     const int32_t* __restrict__ row_assign,
                     const float* __restrict__ row_weight, int E, uint4* __restrict__ dyw,
-                    uint4* __restrict__ dy_b, float4* __restrict__ dx, float* __restrict__ dtopk) {
+                    uint4* __restrict__ dy_b, float4* __restrict__ dx, float* __restrict__ dtopk,
+                    int32_t* __restrict__ expert_order) {
   pdl_trigger();
   pdl_wait();
   __shared__ int s_pstart[kMaxExperts + 1];
@@ -358,6 +359,17 @@ __global__ void __launch_bounds__(kPrepThreads)
     }
   }
   __syncthreads();
+  if (expert_order && blockIdx.x == 0) {
+    // experts by decreasing row count, ties by index (E <= blockDim.x): the
+    // dW GEMM hands out the longest contractions first
+    const int e = threadIdx.x;
+    if (e < E) {
+      const int c = s_count[e];
+      int rank = 0;
+      for (int f = 0; f < E; ++f) rank += s_count[f] > c || (s_count[f] == c && f < e);
+      expert_order[rank] = e;
+    }
+  }
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   const int total = s_pstart[E];
@@ -487,13 +499,14 @@ cudaError_t launch_bwd_prep(const float* dy, int N, int K, int k, const int32_t*
                             int32_t* tile_start_dx, int32_t* pstart, const int32_t* row_token,
                             const int32_t* row_assign, const float* row_weight, int E,
                             int S_pad_max, void* dy_b, void* dyw, float* dx, float* dtopk,
-                            cudaStream_t st) {
+                            cudaStream_t st, int32_t* expert_order) {
   const int wpb = kPrepThreads / 32;
   const int blocks = std::max(1, std::min(cdiv(S_pad_max, wpb), num_sms() * (2048 / kPrepThreads)));
   return launch_pdl(bwd_prep_kernel, dim3(blocks), dim3(kPrepThreads), 0, st, dy, N, K, k, counts,
                     start, BM, tiles_n, pad, tile_start_dx, pstart, row_token, row_assign,
                     row_weight, E, static_cast<uint4*>(dyw), static_cast<uint4*>(dy_b),
-                    reinterpret_cast<float4*>(dx), dtopk);
+                    reinterpret_cast<float4*>(dx), dtopk,
+                    expert_order && E <= kPrepThreads ? expert_order : nullptr);
 }
 
 cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* start, int E, int BM,
