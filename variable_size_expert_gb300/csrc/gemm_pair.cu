@@ -610,6 +610,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const int tiles_k = cdiv(p.K, PBM);
   const int tiles_n = cdiv(p.N, PBN);
   const int total = p.E * tiles_k * tiles_n;
+  // This pair's i-th tile.  The tiles are ordered by decreasing contraction
+  // (experts by row count); successive rounds of the persistent grid walk
+  // the pairs in alternating directions (a snake), so each pair's sum of
+  // long and short tiles stays close to the others'.  Increasing in i.
+  auto snake = [&](int i) { return i * npairs + ((i & 1) ? npairs - 1 - pair : pair); };
 
   if (warp >= 6) {
     // ------------------------------------------------ x gather (128 threads per CTA)
@@ -621,7 +626,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     // row tokens of a stage are fetched two stages ahead of its copies, so
     // the dependent loads stay off the issue path.
     struct Cur {
-      int tau, kb, nkb, m, s0, k0;
+      int i, tau, kb, nkb, m, s0, k0;
     };
     auto seek = [&](Cur& cu) {
       while (cu.tau < total) {
@@ -633,13 +638,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           cu.k0 = t.kbo * PBM + static_cast<int>(rank) * CBM;
           return;
         }
-        cu.tau += npairs;
+        cu.tau = snake(++cu.i);
       }
     };
     auto step = [&](Cur& cu) {
       if (++cu.kb >= cu.nkb) {
         cu.kb = 0;
-        cu.tau += npairs;
+        cu.tau = snake(++cu.i);
         seek(cu);
       }
     };
@@ -650,7 +655,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         tk[i] = cu.tau < total && lr < cu.m ? __ldg(p.row_token + cu.s0 + lr) : -1;
       }
     };
-    Cur cur{pair, 0, 1, 0, 0, 0};
+    Cur cur{0, snake(0), 0, 1, 0, 0, 0};
     seek(cur);
     Cur pf = cur;
     int tk0[4], tk1[4], tk2[4];
@@ -708,7 +713,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int tau = pair; ok && tau < total; tau += npairs) {
+      for (int i = 0, tau = snake(0); ok && tau < total; tau = snake(++i)) {
         const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
         const int ps = __ldg(p.pstart + t.e);
         const int n0 = t.nb * PBN + static_cast<int>(rank) * CBN;
@@ -742,7 +747,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (!leader && lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int tau = pair; ok && tau < total; tau += npairs) {
+      for (int i = 0, tau = snake(0); ok && tau < total; tau = snake(++i)) {
         const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
         for (int kb = 0; kb < t.nkb; ++kb, ++it)
           if (!relay_stage<STAGES>(m, full_l, it, wc)) {
@@ -755,7 +760,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t IDESC = idesc_bf16_f32(PBM, PBN, true, true);
       int it = 0, tcount = 0;
       bool ok = true;
-      for (int tau = pair; ok && tau < total; tau += npairs) {
+      for (int i = 0, tau = snake(0); ok && tau < total; tau = snake(++i)) {
         const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
         if (t.nkb == 0) continue;
         const int acc = tcount & 1;
@@ -797,7 +802,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     // for one another.
     const uint32_t stg0 = m.sEpi + warp * 2 * DW_EPI_BUF;
     int tcount = 0, nst = 0;
-    for (int tau = pair; tau < total; tau += npairs) {
+    for (int i = 0, tau = snake(0); tau < total; tau = snake(++i)) {
       const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
       const int kw = t.kbo * PBM + static_cast<int>(rank) * CBM + warp * 32;  // warp's first k
       const int kcol = kw + lane;
