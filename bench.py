@@ -424,7 +424,28 @@ def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
         "tile": [bm, bn],
         "useful_row_fraction": round(float(counts.sum()) / (bm * sum(-(-int(m) // bm) for m in counts)), 4),
         "tiles": tiles, "count_min": int(counts.min()), "count_max": int(counts.max())}
-    del args_, y, r
+    # skewed backward (same inputs + dy): dW's tile costs follow the expert
+    # row counts, the case its longest-first snake schedule is for
+    dys = torch.from_numpy(np.random.default_rng(1).standard_normal((T, N), dtype=np.float32)).to(dev)
+    ev2 = Events(2)
+    h2 = ev2.handles()
+    for _ in range(3):
+        mgg.moe_backward(dys, args_[0], args_[1], r, k)
+    t_dx, t_dw = [], []
+    for _ in range(10):
+        flush.zero_()
+        lib.mgg_set_kernel_events(h2, 2)
+        mgg.moe_backward(dys, args_[0], args_[1], r, k)
+        lib.mgg_set_kernel_events(None, 0)
+        torch.cuda.synchronize()
+        t_dx.append(ev2.ms(0))
+        t_dw.append(ev2.ms(1))
+    res["bwd_skew"] = {
+        "workload": "fused backward on the skewed forward's inputs, dy ~N(0,1) (seed 1)",
+        "dx_gemm_tflops": round(fl / (statistics.mean(t_dx) * 1e-3) / 1e12, 1),
+        "dw_gemm_tflops": round(fl / (statistics.mean(t_dw) * 1e-3) / 1e12, 1),
+        "dw_output_bytes": E * N * K * 4}
+    del args_, y, r, dys
     # gated expert FFN forward (gate+up GEMM with the SiLU-gated epilogue,
     # down GEMM with the scatter-combine), top-2, H = F = 2048
     c = workloads.FFN_TOP2
