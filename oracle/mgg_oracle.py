@@ -28,6 +28,8 @@ __all__ = [
     "schedule_stats", "grouped_gemm", "moe_forward", "moe_forward_unfused",
     "moe_backward", "moe_backward_rows", "moe_backward_dw_rows", "masked_grouped_gemm",
     "moe_loss", "rel_frobenius", "max_abs_ratio", "silu", "moe_ffn_forward",
+    "E4M3_MAX", "e4m3_decode", "e4m3_encode", "quantize_fp8_rows", "grouped_gemm_fp8",
+    "moe_forward_fp8", "masked_grouped_gemm_fp8",
 ]
 
 
@@ -397,6 +399,138 @@ def masked_grouped_gemm(x, W, masked_m, experts=None) -> np.ndarray:
         m = int(masked_m[e])
         if m:
             y[e, :m] = np.asarray(x[e, :m], dtype=np.float64) @ np.asarray(W[e], dtype=np.float64).T
+    return y
+
+
+# --------------------------------------------------------------------------
+# FP8 operands with per-group scales  [P1 §Choosing an implementation: "FP8
+# adds per-group or per-block scale factors that must travel with each
+# group"; P3 §5-6, DeepGEMM as the FP8 grouped GEMM]
+#
+# Reading taken: operands are OCP FP8 E4M3 codes (1 sign, 4 exponent bits
+# with bias 7, 3 mantissa bits; no infinities, largest finite 448) with one
+# float32 scale per row: per token for activations, per (expert, output
+# channel) for weights.  Such scales factor out of the contraction, so the
+# products are sums of code values scaled once per output element.
+# --------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of each e4m3 code (uint8) as float64.
+
+    Bit 7 is the sign, bits 6..3 the exponent field (bias 7), bits 2..0 the
+    mantissa.  Exponent field 0 encodes subnormals m/8 * 2^-6; every other
+    field (1 + m/8) * 2^(field - 7).  The code with all exponent and mantissa
+    bits set (either sign) is NaN; there is no infinity, so the largest
+    finite magnitude is 1.75 * 2^8 = 448.
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    ex = (c >> 3) & 0xF
+    man = c & 7
+    mag = np.where(ex == 0, man * 2.0 ** -9, (1.0 + man / 8.0) * np.exp2(ex - 7.0))
+    out = np.where((c >> 7) == 1, -mag, mag)
+    return np.where((ex == 15) & (man == 7), np.nan, out)
+
+
+# the 127 non-negative finite values in code order (strictly increasing)
+_E4M3_VALUES = e4m3_decode(np.arange(127, dtype=np.uint8))
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """float32 values -> e4m3 codes (uint8), rounding to nearest.
+
+    The nearest representable magnitude is taken; a tie goes to the code
+    whose mantissa ends in 0 (the even one, as IEEE round-to-nearest-even).
+    Magnitudes above 448 saturate to 448 (the format has no infinity).  The
+    sign bit is kept, also where the magnitude rounds to zero.  NaN inputs
+    are not accepted.
+    """
+    v = np.asarray(v, dtype=np.float32).astype(np.float64)
+    if np.isnan(v).any():
+        raise ValueError("e4m3_encode: NaN input")
+    a = np.abs(v)
+    hi = np.minimum(np.searchsorted(_E4M3_VALUES, a, side="left"), 126)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - _E4M3_VALUES[lo]
+    d_hi = _E4M3_VALUES[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(a >= E4M3_MAX, 126, code)
+    return (code | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
+
+
+def quantize_fp8_rows(v):
+    """Per-row e4m3 quantisation: (codes [R, C] uint8, scale [R] float32).
+
+    For row i of the float32 (or bfloat16-valued) matrix v:
+      amax_i  = max_j |v_ij|
+      s_i     = fl32(amax_i / 448), or 1 for an all-zero row
+      q_ij    = e4m3(fl32(v_ij / s_i))
+    so that v_ij ~ decode(q_ij) * s_i and every non-zero row uses the full
+    code range.  Both divisions are float32 (IEEE, round to nearest).
+    """
+    v32 = np.ascontiguousarray(v, dtype=np.float32)
+    if v32.ndim != 2:
+        raise ValueError("quantize_fp8_rows: 2-D input expected")
+    amax = np.abs(v32).max(axis=1) if v32.shape[1] else np.zeros(v32.shape[0], np.float32)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    q = e4m3_encode(v32 / scale[:, None])
+    return q, scale
+
+
+def grouped_gemm_fp8(Aq, a_scale, Wq, w_scale, end_offs) -> np.ndarray:
+    """C[r, n] = a_scale[r] * w_scale[g, n] * sum_k dec(Aq[r, k]) dec(Wq[g, n, k])
+    for the group g whose rows contain r (end offsets as ``grouped_gemm``)."""
+    A = e4m3_decode(Aq)
+    a_scale = np.asarray(a_scale, dtype=np.float64)
+    w_scale = np.asarray(w_scale, dtype=np.float64)
+    N = Wq.shape[1]
+    C = np.zeros((A.shape[0], N))
+    lo = 0
+    for g, hi in enumerate(np.asarray(end_offs, dtype=np.int64)):
+        if hi > lo:
+            acc = A[lo:hi] @ e4m3_decode(Wq[g]).T
+            C[lo:hi] = acc * a_scale[lo:hi, None] * w_scale[g][None, :]
+        lo = hi
+    return C
+
+
+def moe_forward_fp8(xq, x_scale, Wq, w_scale, expert_ids, topk_weights, tokens=None) -> np.ndarray:
+    """y[t, n] = sum_j w[t, j] * x_scale[t] * w_scale[e, n] *
+                 sum_k dec(xq[t, k]) dec(Wq[e, n, k]),  e = ids[t, j]
+    (the fused forward of ``moe_forward`` on e4m3 operands with per-token and
+    per-(expert, channel) scales).  ``tokens`` restricts the rows computed."""
+    ids = np.asarray(expert_ids)
+    w = np.asarray(topk_weights, dtype=np.float64)
+    x_scale = np.asarray(x_scale, dtype=np.float64)
+    w_scale = np.asarray(w_scale, dtype=np.float64)
+    rows = np.arange(ids.shape[0]) if tokens is None else np.asarray(tokens)
+    N = Wq.shape[1]
+    y = np.zeros((len(rows), N))
+    X = e4m3_decode(xq[rows])
+    for e in np.unique(ids[rows]):
+        sel_t, sel_j = np.nonzero(ids[rows] == e)
+        acc = X[sel_t] @ e4m3_decode(Wq[e]).T
+        contrib = acc * (w[rows[sel_t], sel_j] * x_scale[rows[sel_t]])[:, None] * w_scale[e][None, :]
+        np.add.at(y, sel_t, contrib)
+    return y
+
+
+def masked_grouped_gemm_fp8(xq, x_scale, Wq, w_scale, masked_m, experts=None) -> np.ndarray:
+    """y[e, i, n] = x_scale[e, i] * w_scale[e, n] * sum_k dec(xq[e, i, k]) dec(Wq[e, n, k])
+    for i < masked_m[e]; other rows NaN ("not produced"), as
+    ``masked_grouped_gemm``."""
+    E, M_max = len(masked_m), xq.shape[1]
+    N = Wq.shape[1]
+    x_scale = np.asarray(x_scale, dtype=np.float64)
+    w_scale = np.asarray(w_scale, dtype=np.float64)
+    y = np.full((E, M_max, N), np.nan)
+    for e in (range(E) if experts is None else experts):
+        m = int(masked_m[e])
+        if m:
+            acc = e4m3_decode(xq[e, :m]) @ e4m3_decode(Wq[e]).T
+            y[e, :m] = acc * x_scale[e, :m, None] * w_scale[e][None, :]
     return y
 
 
