@@ -482,6 +482,55 @@ def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
         "down_gemm_tflops": round(fl_dn / (statistics.mean(t_dn) * 1e-3) / 1e12, 1),
         "useful_gflop": round((fl_gu + fl_dn) / 1e9, 3)}
     del fargs, yf, hf, rf
+    # e4m3 fused forward on the top-2 workload: x and W quantised per row
+    # (per token, per expert channel); the timed call is route + the fused
+    # GEMM on the codes, the activation quantisation is timed beside it
+    c = workloads.FWD_TOP2
+    p = workloads.moe_problem(**c)
+    T, K, N, E, k = c["T"], c["K"], c["N"], c["E"], c["k"]
+    xb = p["x"].to(dev)
+    xq, sx = mgg.quantize_fp8(xb)
+    wq, sw = mgg.quantize_fp8(p["W"].to(dev))
+    ids8, w8 = p["expert_ids"].to(dev), p["topk_weights"].to(dev)
+    y8 = torch.empty(T, N, device=dev)
+    r8 = mgg.RoutingBuffers.empty(T, k, E, dev)
+    st8 = mgg.new_status(dev)
+    for _ in range(3):
+        mgg.moe_forward_fp8(xq, sx, wq, sw, ids8, w8, status=st8, out=y8, routing=r8)
+    t_all, t_k, t_q = [], [], []
+    for _ in range(10):
+        flush.zero_()
+        lib.mgg_set_kernel_events(h, 1)
+        s0.record()
+        mgg.moe_forward_fp8(xq, sx, wq, sw, ids8, w8, status=st8, out=y8, routing=r8)
+        s1.record()
+        lib.mgg_set_kernel_events(None, 0)
+        torch.cuda.synchronize()
+        t_all.append(s0.elapsed_time(s1))
+        t_k.append(ev.ms(0))
+        flush.zero_()
+        s0.record()
+        mgg.quantize_fp8(xb)
+        s1.record()
+        torch.cuda.synchronize()
+        t_q.append(s0.elapsed_time(s1))
+    if mgg.read_status(st8) != 0:
+        raise RuntimeError("fp8 forward status set")
+    fl = 2.0 * T * k * K * N
+    gemm_tf = fl / (statistics.mean(t_k) * 1e-3) / 1e12
+    peak8 = 2.0 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    res["fp8_forward"] = {
+        "workload": "fused forward on e4m3 codes with per-token and per-(expert, channel) scales, "
+                    "top-2: T=4096, K=N=2048, E=8, k=2, uniform distinct routing; seed 0",
+        "ms": round(statistics.mean(t_all), 4), "gemm_ms": round(statistics.mean(t_k), 4),
+        "tflops": round(fl / (statistics.mean(t_all) * 1e-3) / 1e12, 1),
+        "gemm_tflops": round(gemm_tf, 1),
+        "quantize_x_ms": round(statistics.mean(t_q), 4),
+        "roofline": {"bound": "tensor", "achieved": round(gemm_tf, 1), "peak": round(peak8, 1),
+                     "unit": "TFLOP/s", "frac": round(gemm_tf / peak8, 4),
+                     "peak_source": f"{peak_kind} bf16 dense (burst) x 2, the nominal e4m3/bf16 ratio",
+                     "traffic": None}}
+    del xb, xq, sx, wq, sw, y8, r8
     # masked decode under CUDA-graph replay (inputs 3.8 GB >> L2)
     c = workloads.DECODE
     E, M, K, N = c["E"], c["M_max"], c["K"], c["N"]
@@ -529,7 +578,42 @@ def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
                      "frac": round(gbs / hbm, 4), "peak_source": f"{peak_kind} copy bandwidth",
                      "traffic": load_traffic("masked_decode_gemm")},
         "timing": "CUDA-graph replay, 20 replays"}
-    del W, x, yd, g
+    # the same decode on e4m3 codes (weights quantised per (expert, channel),
+    # activations per row): half the weight bytes to stream
+    xv = torch.nan_to_num(x, nan=0.0)
+    xq, sx = mgg.quantize_fp8(xv)
+    wq, sw = mgg.quantize_fp8(W)
+    del W, x, xv, g
+    torch.cuda.empty_cache()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            mgg.grouped_gemm_masked_fp8(xq, sx, wq, sw, mm, status=st, out=yd)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mgg.grouped_gemm_masked_fp8(xq, sx, wq, sw, mm, status=st, out=yd)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    s0.record()
+    for _ in range(n):
+        g.replay()
+    s1.record()
+    torch.cuda.synchronize()
+    ms8 = s0.elapsed_time(s1) / n
+    if mgg.read_status(st) != 0:
+        raise RuntimeError("fp8 decode status set")
+    nbytes8 = active * N * K + rows * K + rows * N * 4 + active * N * 4 + rows * 4
+    gbs8 = nbytes8 / (ms8 * 1e-3) / 1e9
+    res["fp8_decode"] = {
+        "workload": "masked decode on e4m3 codes (same shapes and masked_m as decode)",
+        "ms": round(ms8, 4), "GB/s": round(gbs8, 1), "algorithmic_bytes": nbytes8,
+        "speedup_vs_bf16": round(ms / ms8, 3),
+        "roofline": {"bound": "hbm", "achieved": round(gbs8, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gbs8 / hbm, 4), "peak_source": f"{peak_kind} copy bandwidth",
+                     "traffic": None},
+        "timing": "CUDA-graph replay, 20 replays"}
+    del xq, sx, wq, sw, yd, g
     torch.cuda.empty_cache()
     # bare grouped GEMM, E=4, K=128, N=96, sizes [37, 0, 128, 91] (latency)
     b = workloads.bare_grouped(**workloads.BARE_E4)

@@ -57,7 +57,10 @@ typedef enum {
   MGG_ERR_CUDA = 6              /* a CUDA runtime/driver call or launch failed */
 } mgg_status;
 
-typedef enum { MGG_BF16 = 0, MGG_F32 = 1 } mgg_dtype;
+/* MGG_FP8_E4M3: OCP FP8 E4M3 codes (uint8; bias 7, no infinities, largest
+ * finite 448) with f32 scales, accepted only by the *_fp8 entry points and
+ * by mgg_route / mgg_tile_config / mgg_workspace_bytes for their tiles. */
+typedef enum { MGG_BF16 = 0, MGG_F32 = 1, MGG_FP8_E4M3 = 2 } mgg_dtype;
 
 typedef enum {
   MGG_LAYOUT_CONTIGUOUS = 0,      /* rows grouped by expert + int32 end offsets */
@@ -257,6 +260,60 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
                             const mgg_routing* routing, int T, int K, int N, int E, int k,
                             mgg_dtype dtype, float* dx, float* dW, float* dtopk,
                             int32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * FP8 operands with per-group scales ("Grouped GEMM for MoE, in depth",
+ * §Choosing an implementation: FP8 adds per-group or per-block scale factors
+ * that must travel with each group).  The reading taken: e4m3 codes with one
+ * f32 scale per row, i.e. per token for activations and per (expert, output
+ * channel) for weights.  Such scales factor out of the contraction, so the
+ * tensor cores contract the raw codes (f32 accumulation) and the epilogue
+ * applies scale_row * scale_col.  Scales that vary along K (per-block) are
+ * not supported.
+ *
+ * Per-row quantisation of a [rows, cols] matrix (bf16 or f32 values):
+ *   scale[i] = max_j |src[i, j]| / 448   (IEEE f32 division; 1 if the row
+ *                                         is all zeros)
+ *   q[i, j]  = e4m3(src[i, j] / scale[i]) (IEEE f32 division, then round to
+ *                                         nearest even, saturating at 448)
+ * so src ~ decode(q) * scale.  Weights W [E, N, K] quantise as E*N rows of K
+ * (scale [E, N]).  cols % 16 == 0; src and q 16-byte aligned.  Finite
+ * inputs only (a NaN yields a NaN code).  Errors: MGG_ERR_INVALID_ARG,
+ * MGG_ERR_DTYPE (src_dtype not BF16/F32), MGG_ERR_ALIGNMENT,
+ * MGG_ERR_UNSUPPORTED_ARCH, MGG_ERR_CUDA.
+ */
+mgg_status mgg_quantize_fp8(const void* src, mgg_dtype src_dtype, int rows, int cols,
+                            uint8_t* q, float* scale, void* stream);
+
+/*
+ * Bare / masked grouped GEMM on e4m3 operands, as mgg_grouped_gemm with
+ *   CONTIGUOUS(_SIZES): C[r, n] = a_scale[r] * w_scale[g, n] * sum_k A[r, k] W[g, n, k]
+ *   MASKED:             C[e, i, n] = a_scale[e * M_max + i] * w_scale[e, n] *
+ *                                    sum_k A[e, i, k] W[e, n, k]   (i < masked_m[e])
+ * A [rows, K] or [E, M_max, K] and W [E, N, K] as e4m3 codes; a_scale [rows]
+ * or [E, M_max] f32; w_scale [E, N] f32 (16-byte aligned).  K % 16 == 0,
+ * N % 8 == 0 (MGG_ERR_ALIGNMENT).  ws as for mgg_grouped_gemm.
+ */
+mgg_status mgg_grouped_gemm_fp8(const uint8_t* A, const float* a_scale, const uint8_t* W,
+                                const float* w_scale, float* C, mgg_layout layout,
+                                const int32_t* offs, int rows_or_Mmax, int E, int N, int K,
+                                int32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Fused MoE forward on e4m3 operands, as mgg_moe_forward with
+ *   y[t, n] = sum_j topk_weights[t, j] * x_scale[t] * w_scale[e, n] *
+ *             sum_k x[t, k] W[e, n, k],   e = expert_ids[t, j]
+ * x [T, K] and W [E, N, K] e4m3 codes; x_scale [T] f32; w_scale [E, N] f32
+ * (16-byte aligned); y [T, N] f32, zeroed by the call.  K % 16 == 0,
+ * N % 8 == 0.  routing as for mgg_moe_forward (tiles of
+ * mgg_tile_config(MGG_OP_FORWARD, MGG_FP8_E4M3)).
+ * ws: mgg_workspace_bytes(MGG_OP_FORWARD, T, k, E, ...).
+ */
+mgg_status mgg_moe_forward_fp8(const uint8_t* x, const float* x_scale, const uint8_t* W,
+                               const float* w_scale, const int32_t* expert_ids,
+                               const float* topk_weights, int T, int K, int N, int E, int k,
+                               float* y, const mgg_routing* routing, int32_t* dev_status,
+                               void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Gated expert FFN forward, one MoE layer ("Grouped GEMM for MoE, in depth",

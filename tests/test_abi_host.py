@@ -24,7 +24,7 @@ def lib():
 def _declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mgg_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(mgg_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_expected_entry_points():

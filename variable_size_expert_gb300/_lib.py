@@ -22,6 +22,7 @@ MGG_ERR_CUDA = 6
 # mgg_dtype
 MGG_BF16 = 0
 MGG_F32 = 1
+MGG_FP8_E4M3 = 2
 # mgg_layout
 MGG_LAYOUT_CONTIGUOUS = 0
 MGG_LAYOUT_MASKED = 1
@@ -44,7 +45,8 @@ MGG_NOALLOC_SCRATCH_BYTES = 1 << 20
 EXPORTS = (
     "mgg_status_string", "mgg_tile_config", "mgg_workspace_bytes", "mgg_route",
     "mgg_grouped_gemm", "mgg_moe_forward", "mgg_moe_backward", "mgg_debug_tile_schedule",
-    "mgg_set_kernel_events", "mgg_route_noalloc", "mgg_moe_ffn_forward",
+    "mgg_set_kernel_events", "mgg_route_noalloc", "mgg_moe_ffn_forward", "mgg_quantize_fp8",
+    "mgg_grouped_gemm_fp8", "mgg_moe_forward_fp8",
 )
 
 
@@ -78,6 +80,10 @@ _SIGS = {
     "mgg_route_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _RP, _P, _P]),
     "mgg_moe_ffn_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _RP, _P,
                                  _P, _SZ, _P]),
+    "mgg_quantize_fp8": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "mgg_grouped_gemm_fp8": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "mgg_moe_forward_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _RP, _P, _P, _SZ,
+                                 _P]),
 }
 
 _lib = None

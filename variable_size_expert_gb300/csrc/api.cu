@@ -82,9 +82,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
-// Forward-path tile shape for a dtype (bf16: one CTA-pair tile).
+// Forward-path tile shape for a dtype (bf16 and e4m3: one CTA-pair tile).
 void rows_tile(mgg_dtype dt, int* BM, int* BN) {
-  if (dt == MGG_BF16) {
+  if (dt == MGG_BF16 || dt == MGG_FP8_E4M3) {
     *BM = kPairBM;
     *BN = kPairBN;
   } else {
@@ -239,6 +239,20 @@ const char* mgg_status_string(mgg_status s) {
 
 mgg_status mgg_tile_config(mgg_op op, mgg_dtype dtype, int* BM, int* BN, int* BK) {
   if (!BM || !BN || !BK) return MGG_ERR_INVALID_ARG;
+  if (dtype == MGG_FP8_E4M3) {  // e4m3 forward paths: 128 codes per pipeline stage
+    if (op == MGG_OP_ROUTE || op == MGG_OP_FORWARD || op == MGG_OP_GROUPED_GEMM) {
+      rows_tile(dtype, BM, BN);
+      *BK = 2 * kBK;
+      return MGG_OK;
+    }
+    if (op == MGG_OP_MASKED) {
+      *BM = kMaskedBM;
+      *BN = kMaskedBI;
+      *BK = 2 * kBK;
+      return MGG_OK;
+    }
+    return MGG_ERR_DTYPE;
+  }
   if (dtype != MGG_BF16 && dtype != MGG_F32) return MGG_ERR_DTYPE;
   const bool bf = dtype == MGG_BF16;
   switch (op) {
@@ -291,7 +305,7 @@ mgg_status mgg_route(const int32_t* expert_ids, const float* topk_weights, int T
     return MGG_ERR_INVALID_ARG;
   if (T < 1 || k < 1 || E < 1 || N < 1 || E > kMaxExperts) return MGG_ERR_INVALID_ARG;
   if (static_cast<long long>(T) * k > (1LL << 30)) return MGG_ERR_INVALID_ARG;
-  if (dtype != MGG_BF16 && dtype != MGG_F32) return MGG_ERR_DTYPE;
+  if (dtype != MGG_BF16 && dtype != MGG_F32 && dtype != MGG_FP8_E4M3) return MGG_ERR_DTYPE;
   if (ws_bytes < route_ws_bytes(T, k, E) || !aligned(ws, 256)) return MGG_ERR_WORKSPACE;
   mgg_status s = check_arch();
   if (s != MGG_OK) return s;
@@ -324,7 +338,16 @@ mgg_status mgg_grouped_gemm(const void* A, const void* W, float* C, mgg_dtype dt
 
   if (layout == MGG_LAYOUT_MASKED) {
     if (rows_or_Mmax > 1 << 20) return MGG_ERR_INVALID_ARG;
-    MaskedParams p{A, offs, E, rows_or_Mmax, N, K, C, dev_status, wait_limit()};
+    MaskedParams p{};
+    p.x = A;
+    p.masked_m = offs;
+    p.E = E;
+    p.M_max = rows_or_Mmax;
+    p.N = N;
+    p.K = K;
+    p.y = C;
+    p.dev_status = dev_status;
+    p.wait_limit = wait_limit();
     if (!bf)
       return from_cuda(timed(0, st, [&] { return launch_masked_f32(p, static_cast<const float*>(W), st); }));
     CUtensorMap tm;
@@ -525,6 +548,133 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   CUtensorMap tm_dw;
   if (!tmap_dw_store(&tm_dw, dW, E, N, K)) return MGG_ERR_CUDA;
   return from_cuda(timed(1, st, [&] { return launch_dw_pair(tm_dyw, tm_dw, q, st); }));
+}
+
+mgg_status mgg_quantize_fp8(const void* src, mgg_dtype src_dtype, int rows, int cols,
+                            uint8_t* q, float* scale, void* stream) {
+  if (!src || !q || !scale) return MGG_ERR_INVALID_ARG;
+  if (rows < 1 || cols < 1) return MGG_ERR_INVALID_ARG;
+  if (src_dtype != MGG_BF16 && src_dtype != MGG_F32) return MGG_ERR_DTYPE;
+  if (cols % 16 != 0 || !aligned(src, 16) || !aligned(q, 16) || !aligned(scale, 4))
+    return MGG_ERR_ALIGNMENT;
+  mgg_status s = check_arch();
+  if (s != MGG_OK) return s;
+  return from_cuda(launch_quantize_fp8(src, src_dtype == MGG_F32, rows, cols, q, scale,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+mgg_status mgg_grouped_gemm_fp8(const uint8_t* A, const float* a_scale, const uint8_t* W,
+                                const float* w_scale, float* C, mgg_layout layout,
+                                const int32_t* offs, int rows_or_Mmax, int E, int N, int K,
+                                int32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  if (!A || !a_scale || !W || !w_scale || !C || !offs || !dev_status) return MGG_ERR_INVALID_ARG;
+  if (rows_or_Mmax < 1 || E < 1 || N < 1 || K < 1 || E > kMaxExperts) return MGG_ERR_INVALID_ARG;
+  if (layout != MGG_LAYOUT_CONTIGUOUS && layout != MGG_LAYOUT_MASKED &&
+      layout != MGG_LAYOUT_CONTIGUOUS_SIZES)
+    return MGG_ERR_DTYPE;
+  if (K % 16 != 0 || N % 8 != 0) return MGG_ERR_ALIGNMENT;
+  if (!aligned(A, 16) || !aligned(W, 16) || !aligned(C, 16) || !aligned(w_scale, 16) ||
+      !aligned(a_scale, 4))
+    return MGG_ERR_ALIGNMENT;
+  mgg_status s = check_arch();
+  if (s != MGG_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the loads move e4m3 rows as 16-bit units: K codes = K / 2 units
+  const int Ku = K / 2;
+
+  if (layout == MGG_LAYOUT_MASKED) {
+    if (rows_or_Mmax > 1 << 20) return MGG_ERR_INVALID_ARG;
+    MaskedParams p{};
+    p.x = A;
+    p.masked_m = offs;
+    p.E = E;
+    p.M_max = rows_or_Mmax;
+    p.N = N;
+    p.K = Ku;
+    p.y = C;
+    p.x_scale = a_scale;
+    p.w_scale = w_scale;
+    p.dev_status = dev_status;
+    p.wait_limit = wait_limit();
+    CUtensorMap tm;
+    if (!tmap_weights(&tm, W, E, N, Ku, kBK, kMaskedBM)) return MGG_ERR_CUDA;
+    return from_cuda(timed(0, st, [&] { return launch_masked_gemm(tm, p, st, true); }));
+  }
+
+  const size_t need = mgg_workspace_bytes(MGG_OP_GROUPED_GEMM, 0, 0, E, N, K, MGG_FP8_E4M3);
+  if (!ws || ws_bytes < need || !aligned(ws, 256)) return MGG_ERR_WORKSPACE;
+  int32_t* start = at<int32_t>(ws, 0);
+  int32_t* tile_start = at<int32_t>(ws, round256((E + 1) * sizeof(int32_t)));
+  cudaError_t e = launch_offsets_scan(offs, layout == MGG_LAYOUT_CONTIGUOUS_SIZES, E, rows_or_Mmax,
+                                      kPairBM, cdiv(N, kPairBN), start, tile_start, dev_status, st);
+  if (e != cudaSuccess) return MGG_ERR_CUDA;
+  RowsParams p{};
+  p.A = A;
+  p.lda = Ku;
+  p.Kc = Ku;
+  p.row_token = nullptr;
+  p.tile_start = tile_start;
+  p.start = start;
+  p.E = E;
+  p.Nout = N;
+  p.out = C;
+  p.ldo = N;
+  p.a_scale = a_scale;
+  p.b_scale = w_scale;
+  p.dev_status = dev_status;
+  p.wait_limit = wait_limit();
+  CUtensorMap tm, ta;
+  if (!tmap_weights(&tm, W, E, N, Ku, kBK, kPairBN / 2)) return MGG_ERR_CUDA;
+  if (!tmap_rows(&ta, A, rows_or_Mmax, Ku, kPairBM / 2)) return MGG_ERR_CUDA;
+  return from_cuda(
+      timed(0, st, [&] { return launch_rows_pair(kModeBare, false, ta, tm, p, st, true); }));
+}
+
+mgg_status mgg_moe_forward_fp8(const uint8_t* x, const float* x_scale, const uint8_t* W,
+                               const float* w_scale, const int32_t* expert_ids,
+                               const float* topk_weights, int T, int K, int N, int E, int k,
+                               float* y, const mgg_routing* routing, int32_t* dev_status,
+                               void* ws, size_t ws_bytes, void* stream) {
+  if (!x || !x_scale || !W || !w_scale || !expert_ids || !topk_weights || !y ||
+      !routing_ok(routing) || !dev_status || !ws)
+    return MGG_ERR_INVALID_ARG;
+  if (T < 1 || K < 1 || N < 1 || E < 1 || k < 1 || E > kMaxExperts) return MGG_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * k > (1LL << 30)) return MGG_ERR_INVALID_ARG;
+  if (K % 16 != 0 || N % 8 != 0) return MGG_ERR_ALIGNMENT;
+  if (!aligned(x, 16) || !aligned(W, 16) || !aligned(y, 16) || !aligned(w_scale, 16) ||
+      !aligned(x_scale, 4))
+    return MGG_ERR_ALIGNMENT;
+  if (ws_bytes < route_ws_bytes(T, k, E) || !aligned(ws, 256)) return MGG_ERR_WORKSPACE;
+  mgg_status s = check_arch();
+  if (s != MGG_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_route(expert_ids, topk_weights, T, k, E, kPairBM, cdiv(N, kPairBN),
+                               routing->counts, routing->end_offs, routing->start,
+                               routing->tile_start, routing->row_assign, routing->row_token,
+                               routing->row_weight, dev_status, ws, st, y,
+                               static_cast<size_t>(T) * N);
+  if (e != cudaSuccess) return MGG_ERR_CUDA;
+  const int Ku = K / 2;  // e4m3 rows move as 16-bit units
+  RowsParams p{};
+  p.A = x;
+  p.lda = Ku;
+  p.Kc = Ku;
+  p.row_token = routing->row_token;
+  p.row_weight = routing->row_weight;
+  p.tile_start = routing->tile_start;
+  p.start = routing->start;
+  p.E = E;
+  p.Nout = N;
+  p.out = y;
+  p.ldo = N;
+  p.a_scale = x_scale;
+  p.b_scale = w_scale;
+  p.dev_status = dev_status;
+  p.wait_limit = wait_limit();
+  CUtensorMap tm;
+  if (!tmap_weights(&tm, W, E, N, Ku, kBK, kPairBN / 2)) return MGG_ERR_CUDA;
+  return from_cuda(
+      timed(0, st, [&] { return launch_rows_pair(kModeFused, false, tm, tm, p, st, true); }));
 }
 
 mgg_status mgg_moe_ffn_forward(const void* x, const void* Wg, const void* Wu, const void* Wd,

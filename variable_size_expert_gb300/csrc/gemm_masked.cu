@@ -57,6 +57,10 @@ __device__ __forceinline__ MTile decode_masked(int tau, int tiles_n, int tiles_i
   return t;
 }
 
+// F8: e4m3 operands.  Rows still move as 128-byte pieces per stage (128
+// codes, addressed as 16-bit units), the MMA is kind::f8f6f4 and the
+// epilogue multiplies by the weight row's and the activation row's scales.
+template <bool F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     masked_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const MaskedParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -191,7 +195,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x) {
         const MTile t = decode_masked(tau, tiles_n, tiles_i, p);
         if (t.m == 0) continue;
-        const uint32_t idesc = idesc_bf16_f32(BM, cdiv(t.m, 16) * 16, false, false);
+        const int nmma = cdiv(t.m, 16) * 16;
+        const uint32_t idesc =
+            F8 ? idesc_e4m3_f32(BM, nmma, false, false) : idesc_bf16_f32(BM, nmma, false, false);
         const int acc = tcount & 1;
         const uint32_t use = tcount >> 1;
         if (!wait_bar(acc_empty + 8 * acc, (use & 1) ^ 1, wc)) break;
@@ -208,9 +214,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t w0 = sW + s * W_STAGE;
           const uint32_t x0 = sX + s * X_STAGE;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            tc_mma_bf16(d, sw128_desc(w0 + kk * 32, 16, 1024), sw128_desc(x0 + kk * 32, 16, 1024),
-                        idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t wd = sw128_desc(w0 + kk * 32, 16, 1024);
+            const uint64_t xd = sw128_desc(x0 + kk * 32, 16, 1024);
+            if (F8)
+              tc_mma_f8(d, wd, xd, idesc, (kb | kk) != 0);
+            else
+              tc_mma_bf16(d, wd, xd, idesc, (kb | kk) != 0);
+          }
           tc_commit(empty + 8 * s);
           ++it;
         }
@@ -235,6 +246,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float* yrow = p.y + (static_cast<long long>(t.e) * p.M_max + static_cast<long long>(t.ib) * BI) * p.N + n;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BI;
       const int nchunks = cdiv(t.m, 16);
+      const float ws = F8 && n < p.N ? __ldg(p.w_scale + static_cast<long long>(t.e) * p.N + n) : 1.f;
+      const float* xs = F8 ? p.x_scale + static_cast<long long>(t.e) * p.M_max + t.ib * BI : nullptr;
 #pragma unroll 1
       for (int cc = 0; cc < nchunks; ++cc) {
         float v[16];
@@ -243,7 +256,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (n < p.N) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            if (cc * 16 + i < t.m) yrow[static_cast<long long>(cc * 16 + i) * p.N] = v[i];
+            if (cc * 16 + i < t.m)
+              yrow[static_cast<long long>(cc * 16 + i) * p.N] =
+                  F8 ? v[i] * ws * __ldg(xs + cc * 16 + i) : v[i];
         }
       }
       tc_fence_before();
@@ -263,19 +278,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace
 
-cudaError_t launch_masked_gemm(const CUtensorMap& tmap_w, const MaskedParams& p, cudaStream_t st) {
+template <bool F8>
+cudaError_t launch_masked_t(const CUtensorMap& tmap_w, const MaskedParams& p, cudaStream_t st) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(masked_gemm_kernel,
+    cudaError_t e = cudaFuncSetAttribute(masked_gemm_kernel<F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  masked_gemm_kernel<<<num_sms(), NUM_THREADS, SMEM_BYTES, st>>>(tmap_w, p);
+  masked_gemm_kernel<F8><<<num_sms(), NUM_THREADS, SMEM_BYTES, st>>>(tmap_w, p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_masked_gemm(const CUtensorMap& tmap_w, const MaskedParams& p, cudaStream_t st,
+                               bool f8) {
+  return f8 ? launch_masked_t<true>(tmap_w, p, st) : launch_masked_t<false>(tmap_w, p, st);
 }
 
 }  // namespace mgg

@@ -169,7 +169,11 @@ __device__ __forceinline__ float silu_fast(float v) {
 }
 
 // ====================================================================== rows
-template <int MODE, bool B_MN>
+// F8: e4m3 operands (fused and bare modes, both K-major).  A stage still
+// holds 128-byte rows, now of 128 codes, moved by the same gather and TMA
+// code as 16-bit units; the MMA is kind::f8f6f4 (K = 32 per instruction) and
+// the epilogue applies the row and column scales.
+template <int MODE, bool B_MN, bool F8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     rows_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b, const RowsParams p) {
@@ -178,6 +182,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   constexpr bool GATHER = MODE == kModeFused || MODE == kModeFusedDtopk || MODE == kModeGateUp;
   constexpr bool SCATTER = MODE == kModeFused || MODE == kModeFusedDtopk || MODE == kModeScatter;
   constexpr bool GATEUP = MODE == kModeGateUp;
+  static_assert(!F8 || ((MODE == kModeFused || MODE == kModeBare) && !B_MN),
+                "e4m3 operands: fused and bare modes, K-major");
   extern __shared__ uint8_t smem_raw[];
   constexpr int STAGES = kRowsStages;
   const PairSmem m = carve<STAGES, kRowsEpi>(smem_raw);
@@ -339,8 +345,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
     }
     if (leader && lane == 0) {
-      constexpr uint32_t IDESC = idesc_bf16_f32(PBM, PBN, false, B_MN);
-      constexpr uint32_t IDESC_H = idesc_bf16_f32(PBM, PBN / 2, false, B_MN);
+      constexpr uint32_t IDESC =
+          F8 ? idesc_e4m3_f32(PBM, PBN, false, false) : idesc_bf16_f32(PBM, PBN, false, B_MN);
+      constexpr uint32_t IDESC_H = F8 ? idesc_e4m3_f32(PBM, PBN / 2, false, false)
+                                      : idesc_bf16_f32(PBM, PBN / 2, false, B_MN);
       int it = 0, tcount = 0;
       bool ok = true;
       for (int wi = 0, tau = pair; ok && more(wi, tau); ++wi, tau += npairs) {
@@ -366,7 +374,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             const uint64_t adesc = sw128_desc(a0 + kk * 32, 16, 1024);
             const uint64_t bdesc = B_MN ? sw128_desc(b0 + kk * 16 * 128, CHUNK, 1024)
                                         : sw128_desc(b0 + kk * 32, 16, 1024);
-            tc_mma_bf16_cg2(d, adesc, bdesc, idesc, (kb | kk) != 0);
+            if (F8)
+              tc_mma_f8_cg2(d, adesc, bdesc, idesc, (kb | kk) != 0);
+            else
+              tc_mma_bf16_cg2(d, adesc, bdesc, idesc, (kb | kk) != 0);
           }
           tc_commit_cg2_mc(m.empty + 8 * s, 0x3);
           ++it;
@@ -404,6 +415,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if (SCATTER && r_own < t.rows) {
           o_own = __ldg(p.row_token + t.row0 + r_own);
           w_own = __ldg(p.row_weight + t.row0 + r_own);
+          if (F8) w_own *= __ldg(p.a_scale + o_own);  // routing weight x token scale
+        } else if (F8 && r_own < t.rows) {
+          w_own = __ldg(p.a_scale + t.row0 + r_own);  // row scale
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -491,6 +505,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int col = n0 + cc * 32 + 4 * kq;
         uint2 xn[8];
         if (MODE == kModeFusedDtopk && cc + 1 < nch) fetch_x(cc + 1, xn);
+        // e4m3: the expert's scales of this lane's four output columns
+        float4 cs = make_float4(1.f, 1.f, 1.f, 1.f);
+        if (F8 && col < p.Nout)
+          cs = __ldg(reinterpret_cast<const float4*>(p.b_scale +
+                                                     static_cast<long long>(t.e) * p.Nout + col));
         float v[32];
         tmem_ld32(taddr + cc * 32, v);
         tmem_ld_wait();
@@ -508,11 +527,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int rl = 4 * j + rq;
-          const float4 u = ld_shared_v4(stg + rl * 128 + ((kq ^ (rl & 7)) << 4));
+          float4 u = ld_shared_v4(stg + rl * 128 + ((kq ^ (rl & 7)) << 4));
+          if (F8) {
+            u.x *= cs.x;
+            u.y *= cs.y;
+            u.z *= cs.z;
+            u.w *= cs.w;
+          }
           if (ro + rl < t.rows && col < p.Nout) {
             float* o = p.out + static_cast<long long>(orow[j]) * p.ldo + col;
             if (!SCATTER) {
-              *reinterpret_cast<float4*>(o) = u;
+              *reinterpret_cast<float4*>(o) =
+                  F8 ? make_float4(wgt[j] * u.x, wgt[j] * u.y, wgt[j] * u.z, wgt[j] * u.w) : u;
             } else {
               atomicAdd(reinterpret_cast<float4*>(o),
                         make_float4(wgt[j] * u.x, wgt[j] * u.y, wgt[j] * u.z, wgt[j] * u.w));
@@ -890,10 +916,10 @@ cudaError_t prepare(K kern, size_t smem, bool* done) {
   return cudaSuccess;
 }
 
-template <int MODE, bool B_MN>
+template <int MODE, bool B_MN, bool F8 = false>
 cudaError_t launch_rows_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, const RowsParams& p,
                                cudaStream_t st) {
-  auto kern = rows_pair_kernel<MODE, B_MN>;
+  auto kern = rows_pair_kernel<MODE, B_MN, F8>;
   static bool done[64] = {};
   constexpr size_t smem = smem_bytes<kRowsStages, kRowsEpi>();
   cudaError_t e = prepare(kern, smem, done);
@@ -904,7 +930,15 @@ cudaError_t launch_rows_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
 }  // namespace
 
 cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_a,
-                             const CUtensorMap& tmap_b, const RowsParams& p, cudaStream_t st) {
+                             const CUtensorMap& tmap_b, const RowsParams& p, cudaStream_t st,
+                             bool f8) {
+  if (f8) {
+    if (b_mn_major) return cudaErrorInvalidValue;
+    if (mode == kModeBare) return launch_rows_pair_t<kModeBare, false, true>(tmap_a, tmap_b, p, st);
+    if (mode == kModeFused)
+      return launch_rows_pair_t<kModeFused, false, true>(tmap_a, tmap_b, p, st);
+    return cudaErrorInvalidValue;
+  }
   if (!b_mn_major) {
     if (mode == kModeBare) return launch_rows_pair_t<kModeBare, false>(tmap_a, tmap_b, p, st);
     if (mode == kModeFused) return launch_rows_pair_t<kModeFused, false>(tmap_a, tmap_b, p, st);

@@ -56,6 +56,12 @@ struct RowsParams {
   int b_merged;                // MN-major B: tmap_b is the 4-D chunked view, one box per stage
   void* hout;                  // gate/up: h [S, ldh] bf16, sorted rows
   int ldh;
+  // e4m3 operands (fused and bare modes): A and B rows are moved as 16-bit
+  // units, so lda and Kc count byte pairs; the epilogue multiplies by
+  // a_scale (per token in the fused mode, per row in the bare mode) and by
+  // b_scale[e * Nout + n] (per expert and output column)
+  const float* a_scale;
+  const float* b_scale;
   int32_t* dev_status;
   long long wait_limit;
 };
@@ -84,6 +90,10 @@ struct MaskedParams {
   const int32_t* masked_m;     // [E]
   int E, M_max, N, K;
   float* y;                    // [E, M_max, N]
+  // e4m3 operands: K counts byte pairs (rows move as 16-bit units); the
+  // epilogue multiplies by x_scale[e * M_max + i] and w_scale[e * N + n]
+  const float* x_scale;
+  const float* w_scale;
   int32_t* dev_status;
   long long wait_limit;
 };
@@ -117,13 +127,19 @@ cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* star
                                   int max_tiles, int32_t* out, cudaStream_t st);
 
 // gemm_pair.cu (tcgen05, cta_group::2)
+// f8: e4m3 operands (kModeFused and kModeBare, both K-major)
 cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_a,
-                             const CUtensorMap& tmap_b, const RowsParams& p, cudaStream_t st);
+                             const CUtensorMap& tmap_b, const RowsParams& p, cudaStream_t st,
+                             bool f8 = false);
 // tmap_dw: dW [E][N][K] f32 as a 3-D map, box {32, 32, 1}, no swizzle.
 cudaError_t launch_dw_pair(const CUtensorMap& tmap_dyw, const CUtensorMap& tmap_dw,
                            const DwParams& p, cudaStream_t st);
 // gemm_masked.cu (tcgen05)
-cudaError_t launch_masked_gemm(const CUtensorMap& tmap_w, const MaskedParams& p, cudaStream_t st);
+cudaError_t launch_masked_gemm(const CUtensorMap& tmap_w, const MaskedParams& p, cudaStream_t st,
+                               bool f8 = false);
+// quant.cu: per-row e4m3 quantisation of a [rows, cols] bf16 or f32 matrix
+cudaError_t launch_quantize_fp8(const void* src, bool src_f32, int rows, int cols, uint8_t* q,
+                                float* scale, cudaStream_t st);
 
 // simt_f32.cu (exact f32 path)
 cudaError_t launch_rows_f32(int mode, bool w_transposed, const RowsParams& p, const float* W,

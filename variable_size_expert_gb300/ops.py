@@ -8,7 +8,9 @@ Functions mirror the pages' usage ("grouped-gemm-moe", §Usage):
   moe(x, W, expert_ids, topk_weights)        differentiable fused MoE layer
   grouped_gemm(a, W, group_sizes | end_offs) bare variable-size grouped GEMM
 plus the lower-level calls (route, moe_forward, moe_backward,
-grouped_gemm_masked, debug_tile_schedule).
+grouped_gemm_masked, debug_tile_schedule) and the e4m3 forms with per-row
+scales (quantize_fp8, moe_forward_fp8, grouped_gemm_fp8,
+grouped_gemm_masked_fp8).
 """
 from __future__ import annotations
 
@@ -22,7 +24,8 @@ from . import _lib as L
 __all__ = [
     "RoutingBuffers", "route", "moe_forward", "moe_backward", "moe", "grouped_gemm",
     "grouped_gemm_masked", "debug_tile_schedule", "tile_config", "workspace_bytes",
-    "moe_ffn_forward",
+    "moe_ffn_forward", "quantize_fp8", "moe_forward_fp8", "grouped_gemm_fp8",
+    "grouped_gemm_masked_fp8",
     "new_status", "read_status",
 ]
 
@@ -63,17 +66,23 @@ def read_status(status: torch.Tensor) -> int:
     return int(status.item())
 
 
+def _code_of(dtype: torch.dtype) -> int:
+    if dtype in (torch.uint8, torch.float8_e4m3fn):
+        return L.MGG_FP8_E4M3
+    return L.MGG_BF16 if dtype == torch.bfloat16 else L.MGG_F32
+
+
 def tile_config(op: int, dtype: torch.dtype = torch.bfloat16):
     lib = L.load()
     bm, bn, bk = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    code = L.MGG_BF16 if dtype == torch.bfloat16 else L.MGG_F32
+    code = _code_of(dtype)
     L.check(lib.mgg_tile_config(op, code, ctypes.byref(bm), ctypes.byref(bn), ctypes.byref(bk)),
             "mgg_tile_config")
     return bm.value, bn.value, bk.value
 
 
 def workspace_bytes(op: int, T=0, k=0, E=0, N=0, K=0, dtype=torch.bfloat16) -> int:
-    code = L.MGG_BF16 if dtype == torch.bfloat16 else L.MGG_F32
+    code = _code_of(dtype)
     return int(L.load().mgg_workspace_bytes(op, T, k, E, N, K, code))
 
 
@@ -275,6 +284,107 @@ def grouped_gemm_masked(x: torch.Tensor, W: torch.Tensor, masked_m: torch.Tensor
     L.check(lib.mgg_grouped_gemm(_ptr(x), _ptr(W), _ptr(y), code, L.MGG_LAYOUT_MASKED, _ptr(mm),
                                  M_max, E, N, K, _ptr(st), None, 0, _stream()),
             "mgg_grouped_gemm(masked)")
+    return y
+
+
+# ---------------------------------------------------------------- e4m3
+def _codes(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8)
+    if t.dtype != torch.uint8:
+        raise TypeError("e4m3 operands are uint8 codes (or float8_e4m3fn)")
+    return t
+
+
+def quantize_fp8(src: torch.Tensor):
+    """Per-row e4m3 quantisation of a bfloat16/float32 tensor [..., C]:
+    returns (codes uint8 [..., C], scale float32 [...]) with
+    src ~ decode(codes) * scale[..., None] (mgg_quantize_fp8)."""
+    lib = L.load()
+    code = _dtype_code(src)
+    src = src.contiguous()
+    cols = src.shape[-1]
+    rows = src.numel() // max(cols, 1)
+    q = torch.empty(src.shape, dtype=torch.uint8, device=src.device)
+    scale = torch.empty(src.shape[:-1], dtype=torch.float32, device=src.device)
+    L.check(lib.mgg_quantize_fp8(_ptr(src), code, rows, cols, _ptr(q), _ptr(scale), _stream()),
+            "mgg_quantize_fp8")
+    return q, scale
+
+
+def moe_forward_fp8(xq: torch.Tensor, x_scale: torch.Tensor, Wq: torch.Tensor,
+                    w_scale: torch.Tensor, expert_ids: torch.Tensor, topk_weights: torch.Tensor,
+                    status: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                    routing: RoutingBuffers | None = None, workspace: torch.Tensor | None = None):
+    """Fused MoE forward on e4m3 codes with per-token (x_scale [T]) and
+    per-(expert, channel) (w_scale [E, N]) scales.  Returns (y, routing)."""
+    lib = L.load()
+    xq, Wq = _codes(xq), _codes(Wq)
+    T, K = xq.shape
+    E, N, K2 = Wq.shape
+    if K2 != K:
+        raise ValueError("W must be [E, N, K] with the K of x")
+    ids = _ids_i32(expert_ids).contiguous()
+    w = topk_weights.detach().contiguous().float()
+    k = ids.shape[1]
+    dev = xq.device
+    y = out if out is not None else torch.empty(T, N, dtype=torch.float32, device=dev)
+    r = routing or RoutingBuffers.empty(T, k, E, dev)
+    st = status if status is not None else new_status(dev)
+    nbytes = lib.mgg_workspace_bytes(L.MGG_OP_FORWARD, T, k, E, N, K, L.MGG_FP8_E4M3)
+    ws = workspace if workspace is not None and workspace.numel() >= nbytes else _workspace(nbytes, dev)
+    rs = r.struct()
+    L.check(lib.mgg_moe_forward_fp8(_ptr(xq), _ptr(x_scale.contiguous()), _ptr(Wq),
+                                    _ptr(w_scale.contiguous()), _ptr(ids), _ptr(w), T, K, N, E, k,
+                                    _ptr(y), ctypes.byref(rs), _ptr(st), _ptr(ws), ws.numel(),
+                                    _stream()), "mgg_moe_forward_fp8")
+    return y, r
+
+
+def grouped_gemm_fp8(aq: torch.Tensor, a_scale: torch.Tensor, Wq: torch.Tensor,
+                     w_scale: torch.Tensor, group_sizes: torch.Tensor | None = None,
+                     end_offs: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                     out: torch.Tensor | None = None) -> torch.Tensor:
+    """Bare grouped GEMM on e4m3 codes: out[r] = a_scale[r] w_scale[e] * (a[r] W_e^T)."""
+    lib = L.load()
+    aq, Wq = _codes(aq), _codes(Wq)
+    rows, K = aq.shape
+    E, N, _ = Wq.shape
+    if (group_sizes is None) == (end_offs is None):
+        raise ValueError("give exactly one of group_sizes and end_offs")
+    layout = L.MGG_LAYOUT_CONTIGUOUS_SIZES if group_sizes is not None else L.MGG_LAYOUT_CONTIGUOUS
+    offs = (group_sizes if group_sizes is not None else end_offs)
+    offs = offs.to(device=aq.device, dtype=torch.int32).contiguous()
+    dev = aq.device
+    C = out if out is not None else torch.empty(rows, N, dtype=torch.float32, device=dev)
+    st = status if status is not None else new_status(dev)
+    nbytes = lib.mgg_workspace_bytes(L.MGG_OP_GROUPED_GEMM, 0, 0, E, N, K, L.MGG_FP8_E4M3)
+    ws = _workspace(nbytes, dev)
+    L.check(lib.mgg_grouped_gemm_fp8(_ptr(aq), _ptr(a_scale.contiguous()), _ptr(Wq),
+                                     _ptr(w_scale.contiguous()), _ptr(C), layout, _ptr(offs), rows,
+                                     E, N, K, _ptr(st), _ptr(ws), ws.numel(), _stream()),
+            "mgg_grouped_gemm_fp8")
+    return C
+
+
+def grouped_gemm_masked_fp8(xq: torch.Tensor, x_scale: torch.Tensor, Wq: torch.Tensor,
+                            w_scale: torch.Tensor, masked_m: torch.Tensor,
+                            status: torch.Tensor | None = None,
+                            out: torch.Tensor | None = None) -> torch.Tensor:
+    """Masked decode layout on e4m3 codes: out[e, i] = x_scale[e, i] w_scale[e] *
+    (x[e, i] W_e^T) for i < masked_m[e]; other rows of ``out`` are left as they were."""
+    lib = L.load()
+    xq, Wq = _codes(xq), _codes(Wq)
+    E, M_max, K = xq.shape
+    _, N, _ = Wq.shape
+    dev = xq.device
+    mm = masked_m.to(device=dev, dtype=torch.int32).contiguous()
+    y = out if out is not None else torch.zeros(E, M_max, N, dtype=torch.float32, device=dev)
+    st = status if status is not None else new_status(dev)
+    L.check(lib.mgg_grouped_gemm_fp8(_ptr(xq), _ptr(x_scale.contiguous()), _ptr(Wq),
+                                     _ptr(w_scale.contiguous()), _ptr(y), L.MGG_LAYOUT_MASKED,
+                                     _ptr(mm), M_max, E, N, K, _ptr(st), None, 0, _stream()),
+            "mgg_grouped_gemm_fp8(masked)")
     return y
 
 
