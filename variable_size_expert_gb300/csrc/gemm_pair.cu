@@ -37,7 +37,8 @@
 // Roles per CTA (320 threads): warps 0-3 epilogue, warp 4 TMEM allocation
 // (both CTAs), MMA issue (leader) or the gather relay (peer), warp 5 TMA for
 // B (and A in bare mode), warps 6-9 gather A rows with cp.async (gather
-// modes).
+// modes); the dX GEMM adds a second epilogue group, warps 10-13 (448
+// threads).
 #include <algorithm>
 
 #include "internal.h"
@@ -57,10 +58,14 @@ constexpr int LAG = 3;          // cp.async groups a gather thread keeps in flig
 constexpr int A_STAGE = CBM * BK * 2;  // 16 KB
 constexpr int B_STAGE = CBN * BK * 2;  // 16 KB
 constexpr int CHUNK = 64 * BK * 2;     // one 64-wide MN chunk of 64 K rows
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 320;       // 4 epilogue warps (warps 0-3)
+constexpr int kEpiWarpsHi = 10;        // first warp of a second epilogue group (warps 10-13)
+// The dX GEMM (whose epilogue also gathers x for the d(routing weight) dot)
+// runs eight epilogue warps; the other row modes four.
+constexpr int rows_epi_warps(int mode) { return mode == kModeFusedDtopk ? 8 : 4; }
+constexpr int rows_threads(int mode) { return rows_epi_warps(mode) == 8 ? 448 : NUM_THREADS; }
 constexpr int TMEM_COLS = 2 * PBN;
-constexpr int EPI_WARP = 32 * 32 * 4;  // one warp's 32 x 32 f32 staging block
-constexpr int kRowsEpi = 4 * EPI_WARP;
+constexpr int kRowsEpi = 16 * 1024;    // epilogue staging: 4 warps x 32 x 32 f32 or 8 x 32 x 16
 constexpr int DW_EPI_BUF = 32 * 32 * 4;  // one warp's 32 (n) x 32 (k) f32 block
 constexpr int kDwEpi = 4 * 2 * DW_EPI_BUF;  // double-buffered per epilogue warp
 constexpr int kBarBytes = 256;
@@ -124,7 +129,8 @@ static_assert(LAG < kRowsStages && LAG < kDwStages, "gather lag must be below th
 
 // Barrier set-up, TMEM allocation on both CTAs, cluster-wide handshake.
 template <int STAGES>
-__device__ __forceinline__ uint32_t pair_setup(const PairSmem& m, uint32_t full_count, int warp) {
+__device__ __forceinline__ uint32_t pair_setup(const PairSmem& m, uint32_t full_count, int warp,
+                                               int epi_warps) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(m.full + 8 * s, full_count);
@@ -133,7 +139,7 @@ __device__ __forceinline__ uint32_t pair_setup(const PairSmem& m, uint32_t full_
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(m.acc_full + 8 * a, 1);
-      mbar_init(m.acc_empty + 8 * a, 2 * 4);  // one arrival per epilogue warp
+      mbar_init(m.acc_empty + 8 * a, 2 * epi_warps);  // one arrival per epilogue warp
     }
     mbar_init(m.drain, 1);
     *m.abort_flag = 0;
@@ -174,7 +180,7 @@ __device__ __forceinline__ float silu_fast(float v) {
 // code as 16-bit units; the MMA is kind::f8f6f4 (K = 32 per instruction) and
 // the epilogue applies the row and column scales.
 template <int MODE, bool B_MN, bool F8 = false>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 1)
     rows_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b, const RowsParams p) {
   // A rows gathered through row_token (else loaded in sorted order by TMA);
@@ -184,6 +190,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   constexpr bool GATEUP = MODE == kModeGateUp;
   static_assert(!F8 || ((MODE == kModeFused || MODE == kModeBare) && !B_MN),
                 "e4m3 operands: fused and bare modes, K-major");
+  constexpr int EPW = rows_epi_warps(MODE);  // epilogue warps
+  constexpr int CW = EPW == 8 ? 16 : 32;     // columns per staged block
+  constexpr int LPR = CW / 4;                // lanes per staged row after the transpose
+  constexpr int RSTEP = 32 / LPR;            // rows per store instruction
+  static_assert(EPW * 32 * CW * 4 == kRowsEpi, "staging area");
+  static_assert(!GATEUP || CW == 32, "the gate/up epilogue stages 32-column blocks");
   extern __shared__ uint8_t smem_raw[];
   constexpr int STAGES = kRowsStages;
   const PairSmem m = carve<STAGES, kRowsEpi>(smem_raw);
@@ -199,7 +211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmap_b);
   }
   pdl_trigger();
-  const uint32_t tmem_base = pair_setup<STAGES>(m, GATHER ? 2 : 1, warp);
+  const uint32_t tmem_base = pair_setup<STAGES>(m, GATHER ? 2 : 1, warp, EPW);
   pdl_wait();  // the inputs may be the previous kernel's outputs
   const uint32_t full_l = mapa_shared(m.full, 0);           // leader's full[0]
   const uint32_t acc_empty_l = mapa_shared(m.acc_empty, 0);  // leader's acc_empty[0]
@@ -218,7 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   auto more = [&](int wi, int tau) { return SPLIT ? wi < nwork : tau < total; };
   auto item = [&](int wi, int tau) { return SPLIT ? plan.get(wi) : WorkItem{tau, 0, 1}; };
 
-  if (warp >= 6) {
+  if (warp >= 6 && warp < kEpiWarpsHi) {
     // ------------------------------------------------ A gather (128 threads per CTA)
     if (GATHER) {
       const int q = threadIdx.x - 192;
@@ -390,24 +402,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       wait_bar_drain(m.drain, 0, DRAIN_LIMIT);
     }
   } else {
-    // ------------------------------------------------ epilogue (128 threads per CTA)
-    // Lane i of warp w holds accumulator row 32 w + i of this CTA's half.
-    // Each 32 x 32 block passes through the warp's staging buffer (16-byte
-    // pieces XOR-swizzled by row, so both passes are free of bank
-    // conflicts) and leaves transposed: lane L then owns rows 4 j + L / 8
-    // (j = 0..7), columns 4 (L % 8) .. +3, and every store or atomic add
-    // instruction covers four rows x 128 contiguous bytes.
-    const uint32_t stg = m.sEpi + warp * EPI_WARP;
-    const int ro = static_cast<int>(rank) * CBM + warp * 32;  // first pair-tile row of the warp
-    const int kq = lane & 7;
-    const int rq = lane >> 3;
+    // ------------------------------------------------ epilogue (EPW warps per CTA)
+    // Warp w reads TMEM lanes 32 (w % 4) .. +31, its lane quadrant; lane i
+    // holds row 32 (w % 4) + i of this CTA's half.  With eight epilogue warps
+    // (warps 0-3 and 10-13, the dX GEMM) two warps share each quadrant and
+    // take alternate column blocks.  Each 32-row x CW-column block passes
+    // through the warp's staging buffer (16-byte pieces XOR-swizzled by row,
+    // so both passes are free of bank conflicts) and leaves transposed: lane
+    // L then owns rows L / LPR + RSTEP j (j < LPR), columns 4 (L % LPR) .. +3,
+    // and every store or atomic add instruction covers RSTEP rows x 4 CW
+    // contiguous bytes (CW = 32: four rows x 128 bytes; CW = 16: eight rows x
+    // 64 bytes).
+    const int quad = warp & 3;
+    const int half = (EPW == 8 && warp >= kEpiWarpsHi) ? 1 : 0;
+    const uint32_t stg = m.sEpi + (half * 4 + quad) * (32 * CW * 4);
+    const int ro = static_cast<int>(rank) * CBM + quad * 32;  // first pair-tile row of the warp
+    const int kq = lane % LPR;
+    const int rq = lane / LPR;
+    // byte offset of 16-byte piece c of staged row r
+    auto piece = [](int r, int c) {
+      return static_cast<uint32_t>(r * (CW * 4) + ((c ^ ((r >> (LPR == 8 ? 0 : 1)) & (LPR - 1))) << 4));
+    };
     int tcount = 0;
     for (int wi = 0, tau = pair; more(wi, tau); ++wi, tau += npairs) {
       const WorkItem w = item(wi, tau);
       const Tile t = decode_tile(w.tau, p.tile_start, p.start, p.E, PBM);
-      // output row and routing weight of the rows this lane stores
-      int orow[8];
-      float wgt[8];
+      // output row and scale of the rows this lane stores
+      int orow[LPR];
+      float wgt[LPR];
       {
         const int r_own = ro + lane;
         int o_own = t.row0 + r_own;
@@ -420,33 +442,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           w_own = __ldg(p.a_scale + t.row0 + r_own);  // row scale
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          orow[j] = __shfl_sync(0xffffffffu, o_own, 4 * j + rq);
-          wgt[j] = __shfl_sync(0xffffffffu, w_own, 4 * j + rq);
+        for (int j = 0; j < LPR; ++j) {
+          orow[j] = __shfl_sync(0xffffffffu, o_own, rq + RSTEP * j);
+          wgt[j] = __shfl_sync(0xffffffffu, w_own, rq + RSTEP * j);
         }
       }
       const int n0 = t.nb * PBN + (SPLIT ? w.half * (PBN / 2) : 0);
       const int nch =
-          std::min((SPLIT && w.nhalves == 2 ? PBN / 2 : PBN) / 32, cdiv(p.Nout - n0, 32));
-      // x values of the d(routing weight) dot, fetched one 32-column block
-      // ahead (the first before the accumulator wait) to hide their latency
-      uint2 xb[8];
-      auto fetch_x = [&](int cc, uint2(&dst)[8]) {
-        const int col = n0 + cc * 32 + 4 * kq;
+          std::min((SPLIT && w.nhalves == 2 ? PBN / 2 : PBN) / CW, cdiv(p.Nout - n0, CW));
+      // x values of the d(routing weight) dot, fetched one block ahead (the
+      // first before the accumulator wait) to hide their latency
+      uint2 xb[LPR];
+      auto fetch_x = [&](int cc, uint2(&dst)[LPR]) {
+        const int col = n0 + cc * CW + 4 * kq;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          dst[j] = (ro + 4 * j + rq < t.rows && col < p.Nout)
+        for (int j = 0; j < LPR; ++j)
+          dst[j] = (ro + rq + RSTEP * j < t.rows && col < p.Nout)
                        ? __ldg(reinterpret_cast<const uint2*>(
                              static_cast<const __nv_bfloat16*>(p.xdot) +
                              static_cast<long long>(orow[j]) * p.ldx + col))
                        : make_uint2(0u, 0u);
       };
-      if (MODE == kModeFusedDtopk) fetch_x(0, xb);
+      if (MODE == kModeFusedDtopk && half < nch) fetch_x(half, xb);
       const int acc = tcount & 1;
       const uint32_t use = tcount >> 1;
       if (!__all_sync(0xffffffffu, wait_bar(m.acc_full + 8 * acc, use & 1, wc))) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * PBN;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * PBN;
       if (GATEUP) {
         // h = bf16(silu(gate) * up) for the warp's 32 rows and the tile's 128
         // features: accumulator columns c (gate) and 128 + c (up).  Each
@@ -475,16 +497,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                                      silu_fast(g[2 * i + 1]) * u[2 * i + 1]);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              st_shared_v4(stg + lane * 128 + (((hb * 4 + q) ^ (lane & 7)) << 4),
-                           __uint_as_float(hv[4 * q]), __uint_as_float(hv[4 * q + 1]),
-                           __uint_as_float(hv[4 * q + 2]), __uint_as_float(hv[4 * q + 3]));
+              st_shared_v4(stg + piece(lane, hb * 4 + q), __uint_as_float(hv[4 * q]),
+                           __uint_as_float(hv[4 * q + 1]), __uint_as_float(hv[4 * q + 2]),
+                           __uint_as_float(hv[4 * q + 3]));
           }
           __syncwarp();
           const int col = f0 + cp * 64 + 8 * kq;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int rl = 4 * j + rq;
-            const float4 v = ld_shared_v4(stg + rl * 128 + ((kq ^ (rl & 7)) << 4));
+          for (int j = 0; j < LPR; ++j) {
+            const int rl = rq + RSTEP * j;
+            const float4 v = ld_shared_v4(stg + piece(rl, kq));
             if (ro + rl < t.rows && col < p.Nout)
               *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.hout) +
                                         static_cast<long long>(t.row0 + ro + rl) * p.ldh + col) =
@@ -496,38 +518,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         ++tcount;
         continue;
       }
-      float dot[8];
+      float dot[LPR];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) dot[j] = 0.f;
+      for (int j = 0; j < LPR; ++j) dot[j] = 0.f;
       bool released = false;
 #pragma unroll 1
-      for (int cc = 0; cc < nch; ++cc) {
-        const int col = n0 + cc * 32 + 4 * kq;
-        uint2 xn[8];
-        if (MODE == kModeFusedDtopk && cc + 1 < nch) fetch_x(cc + 1, xn);
+      for (int cc = half; cc < nch; cc += EPW / 4) {
+        const int col = n0 + cc * CW + 4 * kq;
+        uint2 xn[LPR];
+        if (MODE == kModeFusedDtopk && cc + EPW / 4 < nch) fetch_x(cc + EPW / 4, xn);
         // e4m3: the expert's scales of this lane's four output columns
         float4 cs = make_float4(1.f, 1.f, 1.f, 1.f);
         if (F8 && col < p.Nout)
           cs = __ldg(reinterpret_cast<const float4*>(p.b_scale +
                                                      static_cast<long long>(t.e) * p.Nout + col));
-        float v[32];
-        tmem_ld32(taddr + cc * 32, v);
+        float v[CW];
+        if constexpr (CW == 32)
+          tmem_ld32(taddr + cc * CW, v);
+        else
+          tmem_ld16(taddr + cc * CW, v);
         tmem_ld_wait();
-        if (cc == nch - 1) {  // accumulator fully read: hand it back to the MMA
+        if (cc + EPW / 4 >= nch) {  // this warp's share read: hand the accumulator back
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
           released = true;
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          st_shared_v4(stg + lane * 128 + ((k ^ (lane & 7)) << 4), v[4 * k], v[4 * k + 1],
-                       v[4 * k + 2], v[4 * k + 3]);
+        for (int k = 0; k < CW / 4; ++k)
+          st_shared_v4(stg + piece(lane, k), v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
         __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int rl = 4 * j + rq;
-          float4 u = ld_shared_v4(stg + rl * 128 + ((kq ^ (rl & 7)) << 4));
+        for (int j = 0; j < LPR; ++j) {
+          const int rl = rq + RSTEP * j;
+          float4 u = ld_shared_v4(stg + piece(rl, kq));
           if (F8) {
             u.x *= cs.x;
             u.y *= cs.y;
@@ -552,9 +576,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
         }
         __syncwarp();  // the block is read before the next one overwrites it
-        if (MODE == kModeFusedDtopk && cc + 1 < nch) {
+        if (MODE == kModeFusedDtopk && cc + EPW / 4 < nch) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) xb[j] = xn[j];
+          for (int j = 0; j < LPR; ++j) xb[j] = xn[j];
         }
       }
       if (!released) {
@@ -563,14 +587,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
       }
       if (MODE == kModeFusedDtopk) {
-        // the eight lanes of a row hold partial sums over their columns
+        // the LPR lanes of a row hold partial sums over their columns (with
+        // eight epilogue warps, both warps of a quadrant add theirs)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < LPR; ++j) {
           float d = dot[j];
-          d += __shfl_xor_sync(0xffffffffu, d, 1);
-          d += __shfl_xor_sync(0xffffffffu, d, 2);
-          d += __shfl_xor_sync(0xffffffffu, d, 4);
-          const int r = ro + 4 * j + rq;
+#pragma unroll
+          for (int o = 1; o < LPR; o <<= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+          const int r = ro + rq + RSTEP * j;
           if (kq == 0 && r < t.rows) atomicAdd(p.dtopk + __ldg(p.row_assign + t.row0 + r), d);
         }
       }
@@ -627,7 +651,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   if (warp == 5 && lane == 0) tma_prefetch_desc(&tmap_dyw);
   if (warp < 4 && lane == 0) tma_prefetch_desc(&tmap_dw);
   pdl_trigger();
-  const uint32_t tmem_base = pair_setup<STAGES>(m, 2, warp);
+  const uint32_t tmem_base = pair_setup<STAGES>(m, 2, warp, 4);
   pdl_wait();  // the inputs may be the previous kernel's outputs
   const uint32_t full_l = mapa_shared(m.full, 0);
   const uint32_t acc_empty_l = mapa_shared(m.acc_empty, 0);
@@ -880,14 +904,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 // Largest grid of co-resident pairs (a persistent kernel must not have
 // clusters waiting for others to finish).
 template <typename K>
-int pair_grid(K kern, size_t smem) {
+int pair_grid(K kern, size_t smem, int threads) {
   static int cache[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && cache[dev]) return cache[dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms() & ~1, 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -924,7 +948,9 @@ cudaError_t launch_rows_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
   constexpr size_t smem = smem_bytes<kRowsStages, kRowsEpi>();
   cudaError_t e = prepare(kern, smem, done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(pair_grid(kern, smem)), dim3(NUM_THREADS), smem, st, ta, tb, p);
+  constexpr int threads = rows_threads(MODE);
+  return launch_pdl(kern, dim3(pair_grid(kern, smem, threads)), dim3(threads), smem, st, ta, tb,
+                    p);
 }
 
 }  // namespace
@@ -958,7 +984,8 @@ cudaError_t launch_dw_pair(const CUtensorMap& tmap_dyw, const CUtensorMap& tmap_
   constexpr size_t smem = smem_bytes<kDwStages, kDwEpi>();
   cudaError_t e = prepare(dw_pair_kernel, smem, done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(dw_pair_kernel, dim3(pair_grid(dw_pair_kernel, smem)), dim3(NUM_THREADS), smem,
+  return launch_pdl(dw_pair_kernel, dim3(pair_grid(dw_pair_kernel, smem, NUM_THREADS)),
+                    dim3(NUM_THREADS), smem,
                     st, tmap_dyw, tmap_dw, p);
 }
 
