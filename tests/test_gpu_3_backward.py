@@ -99,3 +99,25 @@ def test_autograd_function_matches_explicit_calls():
     assert torch.equal(x.grad.float(), dx.to(torch.bfloat16).float())
     assert torch.equal(w.grad, dtopk) or torch.allclose(w.grad, dtopk, rtol=1e-5, atol=1e-6)
     assert W.grad.shape == W.shape
+
+
+@pytest.mark.parametrize("T,K,N,E,k,routing,seed", [
+    (2048, 512, 384, 64, 8, "zipf", 0),     # skewed: long and short contractions, 1-stage tiles
+    (700, 264, 136, 40, 3, "random", 1),     # ragged K and N, empty experts likely
+    (4096, 2048, 2048, 8, 2, "uniform", 2),  # the top-2 shape
+])
+def test_dw_dynamic_schedule_matches_static(T, K, N, E, k, routing, seed, monkeypatch):
+    """dW's tiles taken from the dynamic queue (MGG_DW_SCHEDULE=dynamic) and
+    from the static longest-first snake (the default) give the same bits:
+    every tile is computed whole by one CTA pair, wherever it runs."""
+    p = workloads.moe_problem(T=T, K=K, N=N, E=E, k=k, seed=seed, routing=routing, with_dy=True)
+    monkeypatch.delenv("MGG_DW_SCHEDULE", raising=False)
+    _, dW_static, _ = _run_bwd(p, dW_fill=float("nan"))
+    monkeypatch.setenv("MGG_DW_SCHEDULE", "dynamic")
+    dx, dW_dyn, dt = _run_bwd(p, dW_fill=float("nan"))
+    monkeypatch.delenv("MGG_DW_SCHEDULE")
+    assert torch.equal(dW_static, dW_dyn)
+    if T <= 700:
+        rdx, rdW, rdt = O.moe_backward(p["dy"].numpy(), f64(p["x"]), f64(p["W"]),
+                                       p["expert_ids"].numpy(), p["topk_weights"].numpy())
+        assert_bf16_close(dW_dyn, rdW, "dW dynamic")

@@ -137,8 +137,8 @@ BwdLayout bwd_layout(int T, int k, int E, int N, int K, mgg_dtype dt) {
   off += round256((E + 1) * sizeof(int32_t));
   L.off_pstart = off;
   off += round256((E + 1) * sizeof(int32_t));
-  L.off_order = off;
-  off += round256(E * sizeof(int32_t));
+  L.off_order = off;  // E experts in dW's visiting order + dW's tile counter
+  off += round256((E + 1) * sizeof(int32_t));
   L.S_pad_max = 0;
   if (dt == MGG_BF16) {
     L.off_dy_b = off;
@@ -530,6 +530,14 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   // dW's B operand, the scaled sorted dY [S_pad, N]: same choice over N.
   q.dyw = dyw;
   q.expert_order = order;
+  // dW's tile schedule: the static longest-first snake, or with
+  // MGG_DW_SCHEDULE=dynamic a queue on the counter one past the order (reset
+  // by the prep), measured slower on this GPU
+  {
+    const char* sched = getenv("MGG_DW_SCHEDULE");
+    const bool dyn = sched && sched[0] == 'd';
+    q.tile_counter = order && dyn ? order + E : nullptr;
+  }
   CUtensorMap tm_dyw;
   q.b_merged = 0;
   if (N % 64 == 0) {

@@ -74,6 +74,46 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
   }
 }
 
+// Bounded wait with acquire at cluster scope, for phases that guard plain
+// shared-memory data written by the peer CTA (st.shared::cluster followed by
+// a release arrival), e.g. the dynamic tile ring.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity,
+                                                 const WaitCtl& w) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (*w.abort_flag) return false;
+    if (clock64() - t0 > w.limit) {
+      *w.abort_flag = 1;
+      atomicOr(w.dev_status, kDevTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void st_shared_s32(uint32_t addr, int v) {
+  asm volatile("st.shared.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_s32(uint32_t cluster_addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_shared_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // Wait used only while tearing down (draining copies or MMAs in flight):
 // ignores the abort flag, still bounded.
 __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, long long limit) {

@@ -38,7 +38,7 @@
 // (both CTAs), MMA issue (leader) or the gather relay (peer), warp 5 TMA for
 // B (and A in bare mode), warps 6-9 gather A rows with cp.async (gather
 // modes); the dX GEMM adds a second epilogue group, warps 10-13 (448
-// threads).
+// threads); the dW GEMM adds warp 10, its dynamic tile scheduler (352).
 #include <algorithm>
 
 #include "internal.h"
@@ -60,6 +60,7 @@ constexpr int B_STAGE = CBN * BK * 2;  // 16 KB
 constexpr int CHUNK = 64 * BK * 2;     // one 64-wide MN chunk of 64 K rows
 constexpr int NUM_THREADS = 320;       // 4 epilogue warps (warps 0-3)
 constexpr int kEpiWarpsHi = 10;        // first warp of a second epilogue group (warps 10-13)
+constexpr int DW_THREADS = 352;        // dynamic dW: the 320 above + warp 10, its tile scheduler
 // The dX GEMM (whose epilogue also gathers x for the d(routing weight) dot)
 // runs eight epilogue warps; the other row modes four.
 constexpr int rows_epi_warps(int mode) { return mode == kModeFusedDtopk ? 8 : 4; }
@@ -68,7 +69,8 @@ constexpr int TMEM_COLS = 2 * PBN;
 constexpr int kRowsEpi = 16 * 1024;    // epilogue staging: 4 warps x 32 x 32 f32 or 8 x 32 x 16
 constexpr int DW_EPI_BUF = 32 * 32 * 4;  // one warp's 32 (n) x 32 (k) f32 block
 constexpr int kDwEpi = 4 * 2 * DW_EPI_BUF;  // double-buffered per epilogue warp
-constexpr int kBarBytes = 256;
+constexpr int kBarBytes = 512;
+constexpr int TR = 16;  // dynamic tile ring slots (dW)
 template <int STAGES, int EPI_BYTES>
 constexpr size_t smem_bytes() {
   return 1024 + static_cast<size_t>(STAGES) * (A_STAGE + B_STAGE) + EPI_BYTES + kBarBytes;
@@ -81,14 +83,15 @@ constexpr long long DRAIN_LIMIT = 200000000LL;
 
 struct PairSmem {
   uint32_t sA, sB, sEpi, full, empty, gathered, acc_full, acc_empty, drain;
+  uint32_t tfull, tempty, tids;  // dynamic tile ring: barriers and tile ids
   uint32_t* tmem_slot;
   volatile int* abort_flag;
 };
 
 template <int STAGES, int EPI_BYTES>
 __device__ __forceinline__ PairSmem carve(uint8_t* smem_raw) {
-  constexpr int NUM_BARS = 3 * STAGES + 5;
-  static_assert(NUM_BARS * 8 + 8 <= kBarBytes, "barrier area");
+  constexpr int NUM_BARS = 3 * STAGES + 5 + 2 * TR;
+  static_assert(NUM_BARS * 8 + 8 + 4 * TR <= kBarBytes, "barrier area");
   PairSmem m;
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -103,8 +106,11 @@ __device__ __forceinline__ PairSmem carve(uint8_t* smem_raw) {
   m.acc_full = bar0 + 24 * STAGES;
   m.acc_empty = m.acc_full + 16;
   m.drain = m.acc_full + 32;
+  m.tfull = m.drain + 8;
+  m.tempty = m.tfull + 8 * TR;
   m.tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar0 - base) + 8 * NUM_BARS);
   m.abort_flag = reinterpret_cast<volatile int*>(m.tmem_slot + 1);
+  m.tids = bar0 + 8 * NUM_BARS + 8;
   return m;
 }
 
@@ -130,7 +136,7 @@ static_assert(LAG < kRowsStages && LAG < kDwStages, "gather lag must be below th
 // Barrier set-up, TMEM allocation on both CTAs, cluster-wide handshake.
 template <int STAGES>
 __device__ __forceinline__ uint32_t pair_setup(const PairSmem& m, uint32_t full_count, int warp,
-                                               int epi_warps) {
+                                               int epi_warps, int ring_consumers = 0) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(m.full + 8 * s, full_count);
@@ -142,6 +148,10 @@ __device__ __forceinline__ uint32_t pair_setup(const PairSmem& m, uint32_t full_
       mbar_init(m.acc_empty + 8 * a, 2 * epi_warps);  // one arrival per epilogue warp
     }
     mbar_init(m.drain, 1);
+    for (int r = 0; ring_consumers > 0 && r < TR; ++r) {
+      mbar_init(m.tfull + 8 * r, 1);                   // the scheduler's arrival
+      mbar_init(m.tempty + 8 * r, ring_consumers);     // every consumer of both CTAs
+    }
     *m.abort_flag = 0;
     fence_mbar_init();
   }
@@ -635,7 +645,8 @@ __device__ __forceinline__ DwTile decode_dw(int tau, int tiles_k, int tiles_n,
 // the scaled, expert-sorted dY operand (MN-major, this CTA's 128 n-columns)
 // by TMA.  Rows past m_e are zero-filled on the x side and zero-padded on
 // the dY side.  Tiles of experts with no rows write zeros.
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+template <bool DYN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : NUM_THREADS, 1)
     dw_pair_kernel(const __grid_constant__ CUtensorMap tmap_dyw,
                    const __grid_constant__ CUtensorMap tmap_dw, const DwParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -651,10 +662,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   if (warp == 5 && lane == 0) tma_prefetch_desc(&tmap_dyw);
   if (warp < 4 && lane == 0) tma_prefetch_desc(&tmap_dw);
   pdl_trigger();
-  const uint32_t tmem_base = pair_setup<STAGES>(m, 2, warp, 4);
+  // Dynamic schedule (launched only with a tile counter and the expert
+  // order, which puts the experts with rows first)
+  constexpr bool dyn = DYN;
+  // ring consumers per slot: 4 gather warps, the TMA thread, the MMA or
+  // relay thread and 4 epilogue warps, in each CTA
+  const uint32_t tmem_base = pair_setup<STAGES>(m, 2, warp, 4, dyn ? 2 * 10 : 0);
   pdl_wait();  // the inputs may be the previous kernel's outputs
   const uint32_t full_l = mapa_shared(m.full, 0);
   const uint32_t acc_empty_l = mapa_shared(m.acc_empty, 0);
+  const uint32_t tempty_l = mapa_shared(m.tempty, 0);
 
   const WaitCtl wc{m.abort_flag, p.dev_status, p.wait_limit};
   const int tiles_k = cdiv(p.K, PBM);
@@ -665,13 +682,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   // the pairs in alternating directions (a snake), so each pair's sum of
   // long and short tiles stays close to the others'.  Increasing in i.
   auto snake = [&](int i) { return i * npairs + ((i & 1) ? npairs - 1 - pair : pair); };
+  // Dynamic schedule (f4): the leader's scheduler thread takes the live
+  // tiles (experts with rows, which the longest-first order puts first) off
+  // a global counter and hands them to every role of both CTAs through a
+  // ring of TR slots, so a pair takes its next tile when it is ready for it
+  // (greedy list scheduling); the epilogue warps zero the tiles of experts
+  // without rows on a static stride.
+  int live_tiles = total;
+  if (dyn) {
+    int live = 0;
+    for (int e = 0; e < p.E; ++e) live += __ldg(p.counts + e) > 0;
+    live_tiles = live * tiles_k * tiles_n;
+  }
+  // i-th tile of this role's sequence from the ring (total at its end or on
+  // a timeout).  A whole warp waits and reads; lane 0 (or the single
+  // thread) releases the slot to the scheduler.
+  auto ring_get = [&](int i, bool whole_warp) -> int {
+    const int r = i % TR;
+    const uint32_t ph = (i / TR) & 1;
+    const bool ok = whole_warp ? __all_sync(0xffffffffu, wait_bar_cluster(m.tfull + 8 * r, ph, wc))
+                               : wait_bar_cluster(m.tfull + 8 * r, ph, wc);
+    if (!ok) return total;
+    const int tau = ld_shared_s32(m.tids + 4 * r);
+    const int out = tau < 0 ? total : tau;
+    if (whole_warp) __syncwarp();
+    // relaxed: a release here would make the gather warps wait for their
+    // cp.async copies in flight at every tile; the id has been read (and
+    // used) by now, which is all the scheduler's rewrite must wait for
+    if (!whole_warp || lane == 0) mbar_arrive_cluster_relaxed(tempty_l + 8 * r);
+    return out;
+  };
+  // the sequence of a single-thread role
+  auto seq1 = [&](int i) { return dyn ? ring_get(i, false) : snake(i); };
 
-  if (warp >= 6) {
+  if (warp == 10) {
+    // ------------------------------------------------ tile scheduler (dynamic schedule)
+    if (leader && lane == 0) {
+      const uint32_t tids_p = mapa_shared(m.tids, 1);
+      const uint32_t tfull_p = mapa_shared(m.tfull, 1);
+      const uint32_t tfull_l = mapa_shared(m.tfull, 0);
+      for (int i = 0;; ++i) {
+        const int r = i % TR;
+        if (!wait_bar_cluster(m.tempty + 8 * r, ((i / TR) & 1) ^ 1, wc)) break;
+        const int t = atomicAdd(p.tile_counter, 1);
+        const int tau = t < live_tiles ? t : -1;
+        st_shared_s32(m.tids + 4 * r, tau);
+        st_cluster_s32(tids_p + 4 * r, tau);
+        mbar_arrive_cluster(tfull_l + 8 * r);
+        mbar_arrive_cluster(tfull_p + 8 * r);
+        if (tau < 0) break;
+      }
+    }
+  } else if (warp >= 6) {
     // ------------------------------------------------ x gather (128 threads per CTA)
     const int q = threadIdx.x - 192;
     const int c = q & 7;
     const int rr = q >> 3;  // rows rr + 16 i (i = 0..3) of the stage, both k chunks
     const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(p.x);
+    // The warp's tile sequence; with the dynamic schedule the ids read from
+    // the ring are kept for the cursors below (at most two tiles apart).
+    int hist[4];
+    int nread = 0;
+    auto seq = [&](int i) -> int {
+      if (!dyn) return snake(i);
+      while (nread <= i) {
+        if (nread > 0 && hist[(nread - 1) & 3] >= total) return total;
+        hist[nread & 3] = ring_get(nread, true);
+        ++nread;
+      }
+      return hist[i & 3];
+    };
     // Stage cursor over (tile, k-block), skipping experts with no rows.  The
     // row tokens of a stage are fetched two stages ahead of its copies, so
     // the dependent loads stay off the issue path.
@@ -688,13 +768,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           cu.k0 = t.kbo * PBM + static_cast<int>(rank) * CBM;
           return;
         }
-        cu.tau = snake(++cu.i);
+        cu.tau = seq(++cu.i);
       }
     };
     auto step = [&](Cur& cu) {
       if (++cu.kb >= cu.nkb) {
         cu.kb = 0;
-        cu.tau = snake(++cu.i);
+        cu.tau = seq(++cu.i);
         seek(cu);
       }
     };
@@ -705,7 +785,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         tk[i] = cu.tau < total && lr < cu.m ? __ldg(p.row_token + cu.s0 + lr) : -1;
       }
     };
-    Cur cur{0, snake(0), 0, 1, 0, 0, 0};
+    Cur cur{0, seq(0), 0, 1, 0, 0, 0};
     seek(cur);
     Cur pf = cur;
     int tk0[4], tk1[4], tk2[4];
@@ -763,7 +843,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int i = 0, tau = snake(0); ok && tau < total; tau = snake(++i)) {
+      for (int i = 0, tau = seq1(0); ok && tau < total; tau = seq1(++i)) {
         const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
         const int ps = __ldg(p.pstart + t.e);
         const int n0 = t.nb * PBN + static_cast<int>(rank) * CBN;
@@ -797,7 +877,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (!leader && lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int i = 0, tau = snake(0); ok && tau < total; tau = snake(++i)) {
+      for (int i = 0, tau = seq1(0); ok && tau < total; tau = seq1(++i)) {
         const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
         for (int kb = 0; kb < t.nkb; ++kb, ++it)
           if (!relay_stage<STAGES>(m, full_l, it, wc)) {
@@ -810,7 +890,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t IDESC = idesc_bf16_f32(PBM, PBN, true, true);
       int it = 0, tcount = 0;
       bool ok = true;
-      for (int i = 0, tau = snake(0); ok && tau < total; tau = snake(++i)) {
+      for (int i = 0, tau = seq1(0); ok && tau < total; tau = seq1(++i)) {
         const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
         if (t.nkb == 0) continue;
         const int acc = tcount & 1;
@@ -852,7 +932,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     // for one another.
     const uint32_t stg0 = m.sEpi + warp * 2 * DW_EPI_BUF;
     int tcount = 0, nst = 0;
-    for (int i = 0, tau = snake(0); tau < total; tau = snake(++i)) {
+    // the live tiles from the ring, then (dynamic) the empty experts' tiles
+    int ei = 0, estat = live_tiles + pair;
+    bool ring_done = !dyn;
+    auto enext = [&]() -> int {
+      if (!dyn) return snake(ei++);
+      if (!ring_done) {
+        const int t = ring_get(ei++, true);
+        if (t < total) return t;
+        ring_done = true;
+      }
+      const int t = estat;
+      estat += npairs;
+      return t;
+    };
+    for (int tau = enext(); tau < total; tau = enext()) {
       const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
       const int kw = t.kbo * PBM + static_cast<int>(rank) * CBM + warp * 32;  // warp's first k
       const int kcol = kw + lane;
@@ -953,6 +1047,18 @@ cudaError_t launch_rows_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
                     p);
 }
 
+template <bool DYN>
+cudaError_t launch_dw_pair_t(const CUtensorMap& tmap_dyw, const CUtensorMap& tmap_dw,
+                             const DwParams& p, cudaStream_t st) {
+  static bool done[64] = {};
+  constexpr size_t smem = smem_bytes<kDwStages, kDwEpi>();
+  constexpr int threads = DYN ? DW_THREADS : NUM_THREADS;
+  cudaError_t e = prepare(dw_pair_kernel<DYN>, smem, done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(dw_pair_kernel<DYN>, dim3(pair_grid(dw_pair_kernel<DYN>, smem, threads)),
+                    dim3(threads), smem, st, tmap_dyw, tmap_dw, p);
+}
+
 }  // namespace
 
 cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_a,
@@ -980,13 +1086,8 @@ cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_
 
 cudaError_t launch_dw_pair(const CUtensorMap& tmap_dyw, const CUtensorMap& tmap_dw,
                            const DwParams& p, cudaStream_t st) {
-  static bool done[64] = {};
-  constexpr size_t smem = smem_bytes<kDwStages, kDwEpi>();
-  cudaError_t e = prepare(dw_pair_kernel, smem, done);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(dw_pair_kernel, dim3(pair_grid(dw_pair_kernel, smem, NUM_THREADS)),
-                    dim3(NUM_THREADS), smem,
-                    st, tmap_dyw, tmap_dw, p);
+  if (p.tile_counter && p.expert_order) return launch_dw_pair_t<true>(tmap_dyw, tmap_dw, p, st);
+  return launch_dw_pair_t<false>(tmap_dyw, tmap_dw, p, st);
 }
 
 }  // namespace mgg

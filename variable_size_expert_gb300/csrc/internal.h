@@ -81,6 +81,7 @@ struct DwParams {
   float* dW;                   // [E, N, K]
   int b_merged;                // tmap_dyw is the 3-D chunked view, one box per stage
   const int32_t* expert_order;  // [E] experts by decreasing row count (null: index order)
+  int32_t* tile_counter;       // zeroed counter: dynamic tile queue (null: static schedule)
   int32_t* dev_status;
   long long wait_limit;
 };

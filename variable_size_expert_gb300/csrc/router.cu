@@ -369,6 +369,8 @@ __global__ void __launch_bounds__(kPrepThreads)
       for (int f = 0; f < E; ++f) rank += s_count[f] > c || (s_count[f] == c && f < e);
       expert_order[rank] = e;
     }
+    // one past the order: the dW GEMM's dynamic tile counter, reset here
+    if (threadIdx.x == 0) expert_order[E] = 0;
   }
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
