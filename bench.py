@@ -440,10 +440,31 @@ def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
         torch.cuda.synchronize()
         t_dx.append(ev2.ms(0))
         t_dw.append(ev2.ms(1))
+    # the same dW with the dynamic tile queue (MGG_DW_SCHEDULE=dynamic) in
+    # place of the static longest-first snake
+    prev = os.environ.get("MGG_DW_SCHEDULE")
+    os.environ["MGG_DW_SCHEDULE"] = "dynamic"
+    t_dwd = []
+    try:
+        for _ in range(3):
+            mgg.moe_backward(dys, args_[0], args_[1], r, k)
+        for _ in range(10):
+            flush.zero_()
+            lib.mgg_set_kernel_events(h2, 2)
+            mgg.moe_backward(dys, args_[0], args_[1], r, k)
+            lib.mgg_set_kernel_events(None, 0)
+            torch.cuda.synchronize()
+            t_dwd.append(ev2.ms(1))
+    finally:
+        if prev is None:
+            os.environ.pop("MGG_DW_SCHEDULE", None)
+        else:
+            os.environ["MGG_DW_SCHEDULE"] = prev
     res["bwd_skew"] = {
         "workload": "fused backward on the skewed forward's inputs, dy ~N(0,1) (seed 1)",
         "dx_gemm_tflops": round(fl / (statistics.mean(t_dx) * 1e-3) / 1e12, 1),
         "dw_gemm_tflops": round(fl / (statistics.mean(t_dw) * 1e-3) / 1e12, 1),
+        "dw_gemm_tflops_dynamic_queue": round(fl / (statistics.mean(t_dwd) * 1e-3) / 1e12, 1),
         "dw_output_bytes": E * N * K * 4}
     del args_, y, r, dys
     # gated expert FFN forward (gate+up GEMM with the SiLU-gated epilogue,
