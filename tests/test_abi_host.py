@@ -94,6 +94,44 @@ def test_invalid_arguments_rejected_before_launch(lib):
                                 None, fake, fake, 1 << 30, None) == L.MGG_ERR_INVALID_ARG
 
 
+def test_fp8_invalid_arguments_rejected_before_launch(lib):
+    from variable_size_expert_gb300 import _lib as L
+    fake = ctypes.c_void_p(0x10000)        # never dereferenced: checks fail first
+    r = L.Routing(*([0x10000] * 7))
+    bm, bn, bk = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    assert lib.mgg_tile_config(L.MGG_OP_FORWARD, L.MGG_FP8_E4M3, ctypes.byref(bm), ctypes.byref(bn),
+                               ctypes.byref(bk)) == 0
+    assert (bm.value, bn.value, bk.value) == (256, 256, 128)   # 128 codes per stage row
+    assert lib.mgg_tile_config(L.MGG_OP_BACKWARD, L.MGG_FP8_E4M3, ctypes.byref(bm),
+                               ctypes.byref(bn), ctypes.byref(bk)) == L.MGG_ERR_DTYPE
+    assert lib.mgg_workspace_bytes(L.MGG_OP_BACKWARD, 64, 2, 8, 64, 64, L.MGG_FP8_E4M3) == 0
+    # quantisation: null, columns not a multiple of 16, source dtype
+    assert lib.mgg_quantize_fp8(None, L.MGG_BF16, 4, 16, fake, fake, None) == L.MGG_ERR_INVALID_ARG
+    assert lib.mgg_quantize_fp8(fake, L.MGG_BF16, 4, 24, fake, fake, None) == L.MGG_ERR_ALIGNMENT
+    assert lib.mgg_quantize_fp8(fake, L.MGG_FP8_E4M3, 4, 16, fake, fake,
+                                None) == L.MGG_ERR_DTYPE
+    # fused forward: missing scales, K not a multiple of 16, misaligned weight scales
+    assert lib.mgg_moe_forward_fp8(fake, None, fake, fake, fake, fake, 4, 16, 8, 2, 1, fake,
+                                   ctypes.byref(r), fake, fake, 1 << 20,
+                                   None) == L.MGG_ERR_INVALID_ARG
+    assert lib.mgg_moe_forward_fp8(fake, fake, fake, fake, fake, fake, 4, 24, 8, 2, 1, fake,
+                                   ctypes.byref(r), fake, fake, 1 << 20,
+                                   None) == L.MGG_ERR_ALIGNMENT
+    assert lib.mgg_moe_forward_fp8(fake, fake, fake, ctypes.c_void_p(0x10004), fake, fake, 4, 16,
+                                   8, 2, 1, fake, ctypes.byref(r), fake, fake, 1 << 20,
+                                   None) == L.MGG_ERR_ALIGNMENT
+    # grouped: bad layout, N not a multiple of 8
+    assert lib.mgg_grouped_gemm_fp8(fake, fake, fake, fake, fake, 9, fake, 4, 2, 8, 16, fake, fake,
+                                    1 << 20, None) == L.MGG_ERR_DTYPE
+    assert lib.mgg_grouped_gemm_fp8(fake, fake, fake, fake, fake, 0, fake, 4, 2, 12, 16, fake, fake,
+                                    1 << 20, None) == L.MGG_ERR_ALIGNMENT
+    # the bf16 entry points refuse e4m3 (they carry no scales)
+    assert lib.mgg_moe_forward(fake, fake, fake, fake, 4, 16, 8, 2, 1, L.MGG_FP8_E4M3, fake,
+                               ctypes.byref(r), fake, fake, 1 << 20, None) == L.MGG_ERR_DTYPE
+    assert lib.mgg_grouped_gemm(fake, fake, fake, L.MGG_FP8_E4M3, 0, fake, 4, 2, 8, 16, fake, fake,
+                                1 << 20, None) == L.MGG_ERR_DTYPE
+
+
 def test_product_path_has_no_oracle_or_fallback():
     """The package never imports the oracle, and fails loudly without its library."""
     pkg = os.path.join(ROOT, "variable_size_expert_gb300")

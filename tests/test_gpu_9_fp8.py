@@ -191,3 +191,37 @@ def test_fp8_errors():
                                ws.data_ptr(), ws.numel(), s) == L.MGG_ERR_DTYPE
     torch.cuda.synchronize()
     assert mgg.read_status(st) == 0
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_fp8_forward_and_bare(seed):
+    """Seeded random shapes, ragged against every tile (K a multiple of 16
+    from 16 to 1040, N a multiple of 8 from 8 to 520, 1 to 40 experts, k 1
+    to 4 with repeats): fused forward and bare grouped GEMM on e4m3 codes."""
+    rng = np.random.default_rng(4000 + seed)
+    T = int(rng.integers(1, 701))
+    K = 16 * int(rng.integers(1, 66))
+    N = 8 * int(rng.integers(1, 66))
+    E = int(rng.integers(1, 41))
+    k = int(rng.integers(1, 5))
+    p = workloads.moe_problem(T=T, K=K, N=N, E=E, k=k, seed=seed, routing="random")
+    xq, sx, rxq, rsx = _quant_both(p["x"])
+    wq, sw, rwq, rsw = _quant_both(p["W"])
+    ids, w = p["expert_ids"], p["topk_weights"]
+    st = mgg.new_status(DEV)
+    y, r = mgg.moe_forward_fp8(xq, sx, wq, sw, ids.to(DEV), w.to(DEV), status=st)
+    torch.cuda.synchronize()
+    assert mgg.read_status(st) == 0
+    ref = O.moe_forward_fp8(rxq, rsx, rwq, rsw, ids.numpy(), w.numpy())
+    assert_bf16_close(y, ref, f"fused fp8 {T, K, N, E, k}")
+    sizes = [int(v) for v in rng.integers(0, 200, size=E)]
+    if sum(sizes) == 0:
+        sizes[0] = 1
+    A = workloads.bare_grouped(sizes, K=K, N=N, seed=seed)["A"]
+    aq, sa, raq, rsa = _quant_both(A)
+    C = mgg.grouped_gemm_fp8(aq, sa, wq, sw,
+                             group_sizes=torch.tensor(sizes, dtype=torch.int32, device=DEV), status=st)
+    torch.cuda.synchronize()
+    assert mgg.read_status(st) == 0
+    assert_bf16_close(C, O.grouped_gemm_fp8(raq, rsa, rwq, rsw, O.end_offsets(sizes)),
+                      f"bare fp8 {sizes, K, N}")
