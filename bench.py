@@ -215,7 +215,12 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
 
     # per-kernel pass (not the timed region): the step issued call by call,
-    # CUDA events around each main GEMM on the launching stream
+    # CUDA events around each main GEMM on the launching stream, with dX and
+    # dW one after the other on the whole GPU (MGG_BWD_SPLIT=0) so that each
+    # kernel's rate is against the whole chip; the timed step runs the
+    # library default, dX and dW side by side on disjoint sets of CTA pairs
+    prev_split = os.environ.get("MGG_BWD_SPLIT")
+    os.environ["MGG_BWD_SPLIT"] = "0"
     for _ in range(args.steps):
         if args.flush_mb:
             flush.zero_()
@@ -227,6 +232,10 @@ def run_ours(args, ws, rank, local):
         t_fwd.append(ev_f.ms(0))
         t_dx.append(ev_b.ms(0))
         t_dw.append(ev_b.ms(1))
+    if prev_split is None:
+        os.environ.pop("MGG_BWD_SPLIT", None)
+    else:
+        os.environ["MGG_BWD_SPLIT"] = prev_split
 
     # timed region: exactly K steps, each a replay of the captured step
     barrier(ws)
@@ -281,8 +290,11 @@ def run_ours(args, ws, rank, local):
         "warm_ms_per_step": round(max_over_ranks(statistics.mean(t_warm), ws), 4),
         "config": {"workload": WORKLOAD, "T": T, "K": K, "N": N, "E": E, "k": k,
                    "execution": ("each timed step replays a CUDA graph of the whole step (route, "
-                                 "forward, backward) captured once; eager_ms_per_step is the same step "
-                                 "issued call by call (per-kernel times come from that pass)"),
+                                 "forward, backward) captured once, the backward's dX and dW GEMMs "
+                                 "side by side on disjoint sets of CTA pairs (the library default); "
+                                 "eager_ms_per_step is the same step issued call by call with dX and "
+                                 "dW one after the other on the whole GPU (per-kernel times and the "
+                                 "roofline come from that pass)"),
                    "useful_gflop_per_step": round(flops_step / 1e9, 3),
                    "l2": (f"flushed between timed steps ({args.flush_mb} MiB write)" if args.flush_mb
                           else "not flushed"),
@@ -386,6 +398,58 @@ def run_e2e(args, p, dev, lib, mgg, L, flops_step):
 
 
 def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
+    # per-kernel rates on the whole GPU: dX and dW one after the other
+    prev_split = os.environ.get("MGG_BWD_SPLIT")
+    os.environ["MGG_BWD_SPLIT"] = "0"
+    try:
+        res = _run_extras(dev, mgg, L, lib, peaks, peak_kind, flush)
+    finally:
+        if prev_split is None:
+            os.environ.pop("MGG_BWD_SPLIT", None)
+        else:
+            os.environ["MGG_BWD_SPLIT"] = prev_split
+    res["bwd_split"] = _bwd_split_extra(dev, mgg, flush)
+    return res
+
+
+def _bwd_split_extra(dev, mgg, flush):
+    """The top-2 backward call (prep, dX, dW) with dX and dW one after the
+    other against side by side on disjoint sets of CTA pairs (the default)."""
+    import torch
+    import workloads
+    p = workloads.moe_problem(**workloads.BWD_TOP2)
+    x, W, ids, w, dy = (p[n].to(dev) for n in ("x", "W", "expert_ids", "topk_weights", "dy"))
+    _, r = mgg.moe_forward(x, W, ids, w)
+    k = ids.shape[1]
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out = {"workload": "fused backward of the top-2 workload (bwd_prep + dX + dW), L2 flushed"}
+    prev = os.environ.get("MGG_BWD_SPLIT")
+    try:
+        for name, val in (("serial_ms", "0"), ("side_by_side_ms", None)):
+            if val is None:
+                os.environ.pop("MGG_BWD_SPLIT", None)
+            else:
+                os.environ["MGG_BWD_SPLIT"] = val
+            for _ in range(3):
+                mgg.moe_backward(dy, x, W, r, k)
+            ts = []
+            for _ in range(10):
+                flush.zero_()
+                s0.record()
+                mgg.moe_backward(dy, x, W, r, k)
+                s1.record()
+                torch.cuda.synchronize()
+                ts.append(s0.elapsed_time(s1))
+            out[name] = round(statistics.median(ts), 4)
+    finally:
+        if prev is None:
+            os.environ.pop("MGG_BWD_SPLIT", None)
+        else:
+            os.environ["MGG_BWD_SPLIT"] = prev
+    return out
+
+
+def _run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
     import numpy as np
     import torch
     import workloads

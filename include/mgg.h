@@ -255,6 +255,12 @@ mgg_status mgg_moe_forward(const void* x, const void* W, const int32_t* expert_i
  * dtopk are overwritten.  routing must be the one filled by the forward of
  * the same expert_ids/topk_weights.  ws: mgg_workspace_bytes(MGG_OP_BACKWARD,
  * T, k, E, N, K, dtype).
+ * On the bf16 path the dX and dW GEMMs run side by side on disjoint sets of
+ * the GPU's CTA pairs: the call forks onto a side stream the library creates
+ * once per device (with two events) and joins back to `stream` before it
+ * returns, so stream order and CUDA-graph capture hold as for any call.
+ * The environment variable MGG_BWD_SPLIT (a share of the pairs for dX in
+ * (0, 1), or 0 for one after the other) overrides the split.
  */
 mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
                             const mgg_routing* routing, int T, int K, int N, int E, int k,

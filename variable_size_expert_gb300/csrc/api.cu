@@ -51,6 +51,61 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
 mgg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MGG_OK : MGG_ERR_CUDA; }
 
+// CTA pairs the backward gives dX when it runs dX and dW side by side (the
+// rest go to dW); 0 runs them one after the other.  MGG_BWD_SPLIT overrides:
+// a share in (0, 1), or 0.  Otherwise the split balances the two GEMMs'
+// estimated makespans on P pairs: dX has about (S/256 + E/2) row blocks x
+// ceil(K/256) tiles of N/64 contraction steps, dW E x ceil(K/256) x
+// ceil(N/256) tiles of about S/E/64 steps, each dW step measured about 1.15x
+// a dX step (its output stores).
+int bwd_dx_pairs(int P, long long S, int E, int K, int N) {
+  if (const char* s = getenv("MGG_BWD_SPLIT")) {
+    const double v = atof(s);
+    if (!(v > 0.0 && v < 1.0)) return 0;
+    return std::min(P - 1, std::max(1, static_cast<int>(P * v + 0.5)));
+  }
+  if (P < 2) return 0;
+  const long long tk = cdiv(K, 256), tn = cdiv(N, 256);
+  const long long t_dx = (cdiv(static_cast<int>(std::min<long long>(S, 1LL << 30)), 256) + E / 2) * tk;
+  const long long t_dw = static_cast<long long>(E) * tk * tn;
+  const double c_dx = static_cast<double>(N);
+  const double c_dw = 1.15 * static_cast<double>(S) / E;
+  int best = 0;
+  double best_cost = 0.0;
+  for (int a = 1; a < P; ++a) {
+    const double dx = static_cast<double>((t_dx + a - 1) / a) * c_dx;
+    const double dw = std::max(static_cast<double>((t_dw + (P - a) - 1) / (P - a)),
+                               static_cast<double>(t_dw) / (P - a)) * c_dw;
+    const double cost = std::max(dx, dw);
+    if (best == 0 || cost < best_cost) {
+      best = a;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+// One side stream and a fork/join event pair per device, created on first
+// use and kept (a fork onto it and a join back also capture into a graph).
+struct SideStream {
+  cudaStream_t side;
+  cudaEvent_t fork, join;
+  bool ok;
+};
+SideStream* side_stream() {
+  static SideStream f[kMaxDevices];
+  static std::once_flag once[kMaxDevices];
+  int dev = 0;
+  if (!current_device(&dev)) return nullptr;
+  std::call_once(once[dev], [dev] {
+    SideStream& x = f[dev];
+    x.ok = cudaStreamCreateWithFlags(&x.side, cudaStreamNonBlocking) == cudaSuccess &&
+           cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) == cudaSuccess;
+  });
+  return f[dev].ok ? &f[dev] : nullptr;
+}
+
 // Benchmark instrumentation: event pairs recorded around the main GEMMs.
 thread_local cudaEvent_t t_events[16];
 thread_local int t_nevents = 0;
@@ -523,9 +578,6 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   CUtensorMap tm_wt;
   p.b_merged = K % 64 == 0 && tmap_weights_chunked(&tm_wt, W, E, N, K);
   if (!p.b_merged && !tmap_weights(&tm_wt, W, E, N, K, 64, 64)) return MGG_ERR_CUDA;
-  if (timed(0, st, [&] { return launch_rows_pair(kModeFusedDtopk, true, tm_wt, tm_wt, p, st); }) !=
-      cudaSuccess)
-    return MGG_ERR_CUDA;
 
   // dW's B operand, the scaled sorted dY [S_pad, N]: same choice over N.
   q.dyw = dyw;
@@ -555,7 +607,31 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   }
   CUtensorMap tm_dw;
   if (!tmap_dw_store(&tm_dw, dW, E, N, K)) return MGG_ERR_CUDA;
-  return from_cuda(timed(1, st, [&] { return launch_dw_pair(tm_dyw, tm_dw, q, st); }));
+  auto dx_gemm = [&](cudaStream_t s) {
+    return timed(0, s, [&] { return launch_rows_pair(kModeFusedDtopk, true, tm_wt, tm_wt, p, s); });
+  };
+  auto dw_gemm = [&](cudaStream_t s) {
+    return timed(1, s, [&] { return launch_dw_pair(tm_dyw, tm_dw, q, s); });
+  };
+  const int P = num_sms() / 2;
+  const int pairs_dx = bwd_dx_pairs(P, static_cast<long long>(T) * k, E, K, N);
+  if (pairs_dx <= 0) {
+    if (dx_gemm(st) != cudaSuccess) return MGG_ERR_CUDA;
+    return from_cuda(dw_gemm(st));
+  }
+  // dX and dW side by side on disjoint sets of CTA pairs (a fork onto the
+  // library's side stream and a join back), so one GEMM's ramp-up and tail
+  // overlap the other's work
+  SideStream* f = side_stream();
+  if (!f) return MGG_ERR_CUDA;
+  p.max_pairs = pairs_dx;
+  q.max_pairs = P - pairs_dx;
+  if (cudaEventRecord(f->fork, st) != cudaSuccess ||
+      cudaStreamWaitEvent(f->side, f->fork, 0) != cudaSuccess || dw_gemm(f->side) != cudaSuccess ||
+      dx_gemm(st) != cudaSuccess || cudaEventRecord(f->join, f->side) != cudaSuccess ||
+      cudaStreamWaitEvent(st, f->join, 0) != cudaSuccess)
+    return MGG_ERR_CUDA;
+  return MGG_OK;
 }
 
 mgg_status mgg_quantize_fp8(const void* src, mgg_dtype src_dtype, int rows, int cols,

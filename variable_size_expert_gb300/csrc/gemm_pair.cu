@@ -1043,8 +1043,9 @@ cudaError_t launch_rows_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
   cudaError_t e = prepare(kern, smem, done);
   if (e != cudaSuccess) return e;
   constexpr int threads = rows_threads(MODE);
-  return launch_pdl(kern, dim3(pair_grid(kern, smem, threads)), dim3(threads), smem, st, ta, tb,
-                    p);
+  int grid = pair_grid(kern, smem, threads);
+  if (p.max_pairs > 0) grid = std::min(grid, 2 * p.max_pairs);
+  return launch_pdl(kern, dim3(grid), dim3(threads), smem, st, ta, tb, p);
 }
 
 template <bool DYN>
@@ -1055,8 +1056,9 @@ cudaError_t launch_dw_pair_t(const CUtensorMap& tmap_dyw, const CUtensorMap& tma
   constexpr int threads = DYN ? DW_THREADS : NUM_THREADS;
   cudaError_t e = prepare(dw_pair_kernel<DYN>, smem, done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(dw_pair_kernel<DYN>, dim3(pair_grid(dw_pair_kernel<DYN>, smem, threads)),
-                    dim3(threads), smem, st, tmap_dyw, tmap_dw, p);
+  int grid = pair_grid(dw_pair_kernel<DYN>, smem, threads);
+  if (p.max_pairs > 0) grid = std::min(grid, 2 * p.max_pairs);
+  return launch_pdl(dw_pair_kernel<DYN>, dim3(grid), dim3(threads), smem, st, tmap_dyw, tmap_dw, p);
 }
 
 }  // namespace

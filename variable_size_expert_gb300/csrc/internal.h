@@ -62,6 +62,7 @@ struct RowsParams {
   // b_scale[e * Nout + n] (per expert and output column)
   const float* a_scale;
   const float* b_scale;
+  int max_pairs;               // cap on the persistent grid's CTA pairs (0: all that fit)
   int32_t* dev_status;
   long long wait_limit;
 };
@@ -82,6 +83,7 @@ struct DwParams {
   int b_merged;                // tmap_dyw is the 3-D chunked view, one box per stage
   const int32_t* expert_order;  // [E] experts by decreasing row count (null: index order)
   int32_t* tile_counter;       // zeroed counter: dynamic tile queue (null: static schedule)
+  int max_pairs;               // cap on the persistent grid's CTA pairs (0: all that fit)
   int32_t* dev_status;
   long long wait_limit;
 };
