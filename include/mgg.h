@@ -16,9 +16,12 @@
  * ----------------------------------------
  * - All tensor arguments are DEVICE pointers into memory the caller owns and
  *   keeps alive until the stream work completes.  The library never
- *   allocates, frees or synchronises; everything is enqueued on `stream`
- *   (a cudaStream_t passed as void*, NULL = legacy default stream) in stream
- *   order, so every call can be captured in a CUDA graph.
+ *   allocates or frees device memory and never synchronises; everything is
+ *   enqueued on `stream` (a cudaStream_t passed as void*, NULL = legacy
+ *   default stream) in stream order, so every call can be captured in a
+ *   CUDA graph.  (The bf16 backward forks onto one side stream per device,
+ *   created with its two events on first use, and joins back; see
+ *   mgg_moe_backward.)
  * - Layouts are dense row-major with the shapes given; no strides.
  * - "bf16" tensors hold IEEE bfloat16 bit patterns (uint16); "f32" tensors
  *   hold binary32.  Outputs are always f32 and are fully overwritten by the
