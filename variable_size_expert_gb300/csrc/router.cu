@@ -10,10 +10,15 @@
 // stable counting sort: ties keep ascending assignment index a = t*k + j,
 // the order a stable argsort of the flattened ids gives (same page, §Data
 // layout, offsets and alignment).
+#include <stdlib.h>
+
+#include <cooperative_groups.h>
+
 #include "internal.h"
 #include "schedule.cuh"
 
 namespace mgg {
+namespace cg = cooperative_groups;
 
 namespace {
 
@@ -207,6 +212,117 @@ __global__ void __launch_bounds__(1024)
     }
   }
   if (e == 0) {
+    start[E] = total_rows;
+    tile_start[E] = total_tiles;
+  }
+  __syncthreads();
+  for (int base = a0; base < a1; base += 32) {
+    const int a = base + lane;
+    int id = a < a1 ? __ldg(ids + a) : -1;
+    if (id >= E) id = -1;
+    const unsigned grp = __match_any_sync(0xffffffffu, id);
+    int r = 0;
+    if (id >= 0) r = wc[warp][id] + __popc(grp & lt);
+    __syncwarp();
+    if (id >= 0) {
+      if ((grp & lt) == 0) wc[warp][id] += __popc(grp);
+      row_assign[r] = a;
+      row_token[r] = a / k;
+      row_weight[r] = __ldg(w + a);
+    }
+    __syncwarp();
+  }
+}
+
+// The same router over several blocks in one cooperative launch: routing
+// block b takes the contiguous chunk [b C, (b+1) C) of the assignments
+// (C = kRouteCoopChunk, 32 per warp for the top-2 workload), counts it per
+// warp and expert, publishes its per-expert totals to hist[b][e], and after
+// one grid-wide barrier derives, per expert, the total count (so the
+// offsets and tile prefix sums, written by block 0) and the rows of the
+// blocks before it, which makes the sort stable across blocks as the warp
+// bases make it stable within a block.  The grid's other blocks zero
+// `zero` (y) meanwhile and join the barrier.  All blocks are co-resident
+// (a cooperative launch), so the barrier cannot wait on an unscheduled one.
+constexpr int kRouteCoopChunk = 1024;
+
+__global__ void __launch_bounds__(1024)
+    route_coop_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, int S,
+                      int k, int E, int BM, int tiles_n, int32_t* __restrict__ counts,
+                      int32_t* __restrict__ end_offs, int32_t* __restrict__ start,
+                      int32_t* __restrict__ tile_start, int32_t* __restrict__ row_assign,
+                      int32_t* __restrict__ row_token, float* __restrict__ row_weight,
+                      int32_t* dev_status, int32_t* hist, int nb, float4* __restrict__ zero,
+                      long long nzero4) {
+  pdl_trigger();
+  pdl_wait();  // y, the routing buffers and ids may belong to the previous kernel
+  cg::grid_group grid = cg::this_grid();
+  __shared__ int wc[32][kRouteSmallE];  // per-warp counts, then per-warp bases
+  const int b = blockIdx.x;
+  const bool router = b < nb;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  const int c0 = b * kRouteCoopChunk;
+  const int c1 = min(S, c0 + kRouteCoopChunk);
+  const int L = kRouteCoopChunk / 32;
+  const int a0 = min(c1, c0 + warp * L), a1 = min(c1, a0 + L);
+  if (router) {
+    for (int i = threadIdx.x; i < 32 * kRouteSmallE; i += blockDim.x) (&wc[0][0])[i] = 0;
+    __syncthreads();
+    bool bad = false;
+    for (int base = a0; base < a1; base += 32) {
+      const int a = base + lane;
+      int id = a < a1 ? __ldg(ids + a) : -1;
+      if (a < a1 && (id < 0 || id >= E)) {
+        bad = true;
+        id = -1;
+      }
+      const unsigned grp = __match_any_sync(0xffffffffu, id);
+      if (id >= 0 && (grp & lt) == 0) wc[warp][id] += __popc(grp);
+      __syncwarp();  // the next group leader may be another lane
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(dev_status, kDevBadExpertId);
+    __syncthreads();
+    const int e = threadIdx.x;
+    if (e < E) {
+      int m = 0;
+      for (int v = 0; v < 32; ++v) m += wc[v][e];
+      hist[b * E + e] = m;
+    }
+  } else {
+    const long long stride = static_cast<long long>(gridDim.x - nb) * blockDim.x;
+    for (long long i = static_cast<long long>(b - nb) * blockDim.x + threadIdx.x; i < nzero4;
+         i += stride)
+      zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  grid.sync();  // every block's totals are published
+  if (!router) return;
+  const int e = threadIdx.x;
+  int m = 0, before = 0;
+  if (e < E)
+    for (int bb = 0; bb < nb; ++bb) {
+      const int h = __ldcg(hist + bb * E + e);
+      m += h;
+      before += bb < b ? h : 0;
+    }
+  int total_rows, total_tiles;
+  const int st = block_scan_excl(e < E ? m : 0, 0, AddOp(), &total_rows);
+  const int ts = block_scan_excl(e < E ? cdiv(m, BM) * tiles_n : 0, 0, AddOp(), &total_tiles);
+  if (e < E) {
+    if (b == 0) {
+      counts[e] = m;
+      start[e] = st;
+      end_offs[e] = st + m;
+      tile_start[e] = ts;
+    }
+    int run = st + before;
+    for (int v = 0; v < 32; ++v) {
+      const int c = wc[v][e];
+      wc[v][e] = run;
+      run += c;
+    }
+  }
+  if (e == 0 && b == 0) {
     start[E] = total_rows;
     tile_start[E] = total_tiles;
   }
@@ -443,6 +559,12 @@ __global__ void debug_schedule_kernel(const int32_t* __restrict__ tile_start,
 
 }  // namespace
 
+// The cooperative router (MGG_ROUTER=block selects the single-block one).
+bool route_coop_enabled() {
+  const char* v = getenv("MGG_ROUTER");
+  return !(v && v[0] == 'b');
+}
+
 size_t route_ws_bytes(int T, int k, int E) {
   const size_t S = static_cast<size_t>(T) * k;
   const size_t nchunks = (S + kRouteChunk - 1) / kRouteChunk;
@@ -458,6 +580,30 @@ cudaError_t launch_route(const int32_t* ids, const float* w, int T, int k, int E
   // the single-block router zeroes `zero` with its other blocks (float4 at a
   // time: needs 16-byte alignment and a multiple of 4 floats)
   const bool fuse_zero = zero && zero_floats % 4 == 0 && reinterpret_cast<uintptr_t>(zero) % 16 == 0;
+  if (S <= kRouteSmallS && E <= kRouteSmallE && route_coop_enabled()) {
+    // one cooperative launch: cdiv(S, 1024) routing blocks, the rest of the
+    // GPU (one block per SM in all) zeroing y
+    const int nb = (S + kRouteCoopChunk - 1) / kRouteCoopChunk;
+    const int blocks = fuse_zero && zero_floats > 0 ? std::max(nb + 1, num_sms()) : nb;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(1024);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(
+        &cfg, route_coop_kernel, ids, w, S, k, E, BM, tiles_n, counts, end_offs, start, tile_start,
+        row_assign, row_token, row_weight, dev_status, static_cast<int32_t*>(ws), nb,
+        reinterpret_cast<float4*>(zero), fuse_zero ? static_cast<long long>(zero_floats / 4) : 0LL);
+    if (e == cudaSuccess && zero && !fuse_zero && zero_floats > 0)
+      e = cudaMemsetAsync(zero, 0, zero_floats * sizeof(float), st);
+    return e;
+  }
   if (S <= kRouteSmallS && E <= kRouteSmallE) {
     const int blocks = 1 + (fuse_zero && zero_floats > 0 ? std::max(1, num_sms() - 1) : 0);
     cudaError_t e = launch_pdl(
