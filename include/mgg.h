@@ -103,6 +103,10 @@ typedef enum {
  *   row_assign [S]   int32  sorted row r -> assignment a = t*k + j
  *   row_token  [S]   int32  sorted row r -> token t
  *   row_weight [S]   f32    sorted row r -> topk_weights[t, j]
+ *   assign_row [S]   int32  assignment a -> its sorted row (the inverse of
+ *                           row_assign, -1 for an assignment whose expert id
+ *                           is out of range; "Grouped GEMM", §4.3: permute
+ *                           and un-permute use the same indices, reversed)
  */
 typedef struct {
   int32_t* counts;
@@ -112,6 +116,7 @@ typedef struct {
   int32_t* row_assign;
   int32_t* row_token;
   float* row_weight;
+  int32_t* assign_row;
 } mgg_routing;
 
 /* Human-readable name of a status code (static storage). */

@@ -67,7 +67,7 @@ def test_tile_config_and_workspace(lib):
 def test_invalid_arguments_rejected_before_launch(lib):
     from variable_size_expert_gb300 import _lib as L
     fake = ctypes.c_void_p(0x10000)        # never dereferenced: checks fail first
-    r = L.Routing(*([0x10000] * 7))
+    r = L.Routing(*([0x10000] * 8))
     # null pointers
     assert lib.mgg_moe_forward(None, fake, fake, fake, 4, 8, 8, 2, 1, 0, fake, ctypes.byref(r),
                                fake, fake, 1 << 20, None) == L.MGG_ERR_INVALID_ARG
@@ -97,7 +97,7 @@ def test_invalid_arguments_rejected_before_launch(lib):
 def test_fp8_invalid_arguments_rejected_before_launch(lib):
     from variable_size_expert_gb300 import _lib as L
     fake = ctypes.c_void_p(0x10000)        # never dereferenced: checks fail first
-    r = L.Routing(*([0x10000] * 7))
+    r = L.Routing(*([0x10000] * 8))
     bm, bn, bk = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     assert lib.mgg_tile_config(L.MGG_OP_FORWARD, L.MGG_FP8_E4M3, ctypes.byref(bm), ctypes.byref(bn),
                                ctypes.byref(bk)) == 0

@@ -27,6 +27,9 @@ def _check_routing(r, ids, w, E, N):
     assert np.array_equal(r.row_token.cpu().numpy()[:S], ref.row_token)
     assert np.array_equal(r.row_weight.cpu().numpy()[:S].view(np.uint32),
                           ref.row_weight.astype(np.float32).view(np.uint32))
+    inv = np.full(S, -1, dtype=np.int64)        # assignment -> sorted row
+    inv[ref.row_assign] = np.arange(ref.row_assign.size)
+    assert np.array_equal(r.assign_row.cpu().numpy()[:S], inv)
     sched = O.tile_schedule(ref.counts, N, BM, BN)
     assert np.array_equal(r.tile_start.cpu().numpy(), sched["tile_start"])
     return sched
@@ -87,6 +90,11 @@ def test_route_bad_expert_ids_flagged():
     assert mgg.read_status(st) & mgg._lib.MGG_DEV_BAD_EXPERT_ID
     # the valid assignments are still routed
     assert r.counts.cpu().tolist() == [1, 1, 1, 1]
+    # and the skipped ones (a = 2: -1, a = 5: 7) have no sorted row
+    inv = r.assign_row.cpu().tolist()
+    assert inv[2] == -1 and inv[5] == -1
+    ra = r.row_assign.cpu().tolist()
+    assert all(ra[inv[a]] == a for a in (0, 1, 3, 4))
 
 
 def test_route_graph_capture_replay():

@@ -59,6 +59,7 @@ class Routing(ctypes.Structure):
         ("row_assign", ctypes.c_void_p),
         ("row_token", ctypes.c_void_p),
         ("row_weight", ctypes.c_void_p),
+        ("assign_row", ctypes.c_void_p),
     ]
 
 

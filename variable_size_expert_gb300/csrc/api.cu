@@ -213,7 +213,7 @@ T* at(void* ws, size_t off) {
 
 bool routing_ok(const mgg_routing* r) {
   return r && r->counts && r->end_offs && r->start && r->tile_start && r->row_assign &&
-         r->row_token && r->row_weight;
+         r->row_token && r->row_weight && r->assign_row;
 }
 
 mgg_status check_moe_sizes(int T, int K, int N, int E, int k, mgg_dtype dt) {
@@ -370,7 +370,7 @@ mgg_status mgg_route(const int32_t* expert_ids, const float* topk_weights, int T
   return from_cuda(launch_route(expert_ids, topk_weights, T, k, E, BM, cdiv(N, BN),
                                 routing->counts, routing->end_offs, routing->start,
                                 routing->tile_start, routing->row_assign, routing->row_token,
-                                routing->row_weight, dev_status, ws, st));
+                                routing->row_weight, routing->assign_row, dev_status, ws, st));
 }
 
 mgg_status mgg_grouped_gemm(const void* A, const void* W, float* C, mgg_dtype dtype,
@@ -464,7 +464,7 @@ mgg_status mgg_moe_forward(const void* x, const void* W, const int32_t* expert_i
   cudaError_t e = launch_route(expert_ids, topk_weights, T, k, E, BM, cdiv(N, BN), routing->counts,
                                routing->end_offs, routing->start, routing->tile_start,
                                routing->row_assign, routing->row_token, routing->row_weight,
-                               dev_status, ws, st, y, static_cast<size_t>(T) * N);
+                               routing->assign_row, dev_status, ws, st, y, static_cast<size_t>(T) * N);
   if (e != cudaSuccess) return MGG_ERR_CUDA;
   RowsParams p{};
   p.A = x;
@@ -566,10 +566,9 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   // one pass over dy: the backward schedules (dX tile prefix sums, padded
   // segment starts), the bf16 operands of both GEMMs, and dx, dtopk zeroed
   // for the dX epilogue's atomic adds
-  if (launch_bwd_prep(dy, N, K, k, routing->counts, routing->start, BM, cdiv(K, BN), kDwPad,
-                      tile_start_dx, pstart, routing->row_token, routing->row_assign,
-                      routing->row_weight, E, L.S_pad_max, dy_b, dyw, dx, dtopk, st,
-                      order) != cudaSuccess)
+  if (launch_bwd_prep(dy, T, N, K, k, routing->counts, routing->start, BM, cdiv(K, BN), kDwPad,
+                      tile_start_dx, pstart, routing->assign_row, routing->row_weight, E,
+                      L.S_pad_max, dy_b, dyw, dx, dtopk, st, order) != cudaSuccess)
     return MGG_ERR_CUDA;
   p.A = dy_b;
   // dX reads W_e transposed: per stage each CTA takes 64 contraction rows of
@@ -735,7 +734,7 @@ mgg_status mgg_moe_forward_fp8(const uint8_t* x, const float* x_scale, const uin
   cudaError_t e = launch_route(expert_ids, topk_weights, T, k, E, kPairBM, cdiv(N, kPairBN),
                                routing->counts, routing->end_offs, routing->start,
                                routing->tile_start, routing->row_assign, routing->row_token,
-                               routing->row_weight, dev_status, ws, st, y,
+                               routing->row_weight, routing->assign_row, dev_status, ws, st, y,
                                static_cast<size_t>(T) * N);
   if (e != cudaSuccess) return MGG_ERR_CUDA;
   const int Ku = K / 2;  // e4m3 rows move as 16-bit units
@@ -789,7 +788,7 @@ mgg_status mgg_moe_ffn_forward(const void* x, const void* Wg, const void* Wu, co
   cudaError_t e = launch_route(expert_ids, topk_weights, T, k, E, kPairBM, cdiv(H, kPairBN),
                                routing->counts, routing->end_offs, routing->start,
                                routing->tile_start, routing->row_assign, routing->row_token,
-                               routing->row_weight, dev_status, ws, st, y,
+                               routing->row_weight, routing->assign_row, dev_status, ws, st, y,
                                static_cast<size_t>(T) * H);
   if (e != cudaSuccess) return MGG_ERR_CUDA;
   // the gate/up GEMM's tiles: 256 rows x 128 features (gate and up side by side)

@@ -112,20 +112,20 @@ bool encode_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* d
 cudaError_t launch_route(const int32_t* ids, const float* w, int T, int k, int E, int BM,
                          int tiles_n, int32_t* counts, int32_t* end_offs, int32_t* start,
                          int32_t* tile_start, int32_t* row_assign, int32_t* row_token,
-                         float* row_weight, int32_t* dev_status, void* ws, cudaStream_t st,
-                         float* zero = nullptr, size_t zero_floats = 0);
+                         float* row_weight, int32_t* assign_row, int32_t* dev_status, void* ws,
+                         cudaStream_t st, float* zero = nullptr, size_t zero_floats = 0);
 size_t route_ws_bytes(int T, int k, int E);
 cudaError_t launch_offsets_scan(const int32_t* offs, bool is_sizes, int E, int rows, int BM,
                                 int tiles_n, int32_t* start, int32_t* tile_start,
                                 int32_t* dev_status, cudaStream_t st);
 cudaError_t launch_bwd_scan(const int32_t* counts, int E, int BM, int tiles_n, int pad,
                             int32_t* tile_start_dx, int32_t* pstart, cudaStream_t st);
-cudaError_t launch_bwd_prep(const float* dy, int N, int K, int k, const int32_t* counts,
+cudaError_t launch_bwd_prep(const float* dy, int T, int N, int K, int k, const int32_t* counts,
                             const int32_t* start, int BM, int tiles_n, int pad,
-                            int32_t* tile_start_dx, int32_t* pstart, const int32_t* row_token,
-                            const int32_t* row_assign, const float* row_weight, int E,
-                            int S_pad_max, void* dy_b, void* dyw, float* dx, float* dtopk,
-                            cudaStream_t st, int32_t* expert_order = nullptr);
+                            int32_t* tile_start_dx, int32_t* pstart, const int32_t* assign_row,
+                            const float* row_weight, int E, int S_pad_max, void* dy_b, void* dyw,
+                            float* dx, float* dtopk, cudaStream_t st,
+                            int32_t* expert_order = nullptr);
 cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* start, int E, int BM,
                                   int max_tiles, int32_t* out, cudaStream_t st);
 

@@ -53,7 +53,7 @@ extern "C" mgg_status mgg_route_noalloc(const int32_t* expert_ids, const float* 
   using namespace mgg;
   if (!expert_ids || !topk_weights || !dev_status || !routing || !routing->counts ||
       !routing->end_offs || !routing->start || !routing->tile_start || !routing->row_assign ||
-      !routing->row_token || !routing->row_weight)
+      !routing->row_token || !routing->row_weight || !routing->assign_row)
     return MGG_ERR_INVALID_ARG;
   if (T < 1 || k < 1 || E < 1 || N < 1 || E > kMaxExperts) return MGG_ERR_INVALID_ARG;
   if (static_cast<long long>(T) * k > (1LL << 30)) return MGG_ERR_INVALID_ARG;

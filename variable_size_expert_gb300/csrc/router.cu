@@ -123,7 +123,8 @@ __global__ void route_scatter_kernel(const int32_t* __restrict__ ids,
                                      const int32_t* __restrict__ chunk_first,
                                      int32_t* __restrict__ row_assign,
                                      int32_t* __restrict__ row_token,
-                                     float* __restrict__ row_weight) {
+                                     float* __restrict__ row_weight,
+                                     int32_t* __restrict__ assign_row) {
   __shared__ int sid[kRouteChunk];
   const int a = blockIdx.x * kRouteChunk + threadIdx.x;
   const int id = a < S ? ids[a] : -1;
@@ -136,6 +137,9 @@ __global__ void route_scatter_kernel(const int32_t* __restrict__ ids,
     row_assign[r] = a;
     row_token[r] = a / k;
     row_weight[r] = w[a];
+    assign_row[a] = r;
+  } else if (a < S) {
+    assign_row[a] = -1;
   }
 }
 
@@ -160,7 +164,8 @@ __global__ void __launch_bounds__(1024)
                        int32_t* __restrict__ end_offs, int32_t* __restrict__ start,
                        int32_t* __restrict__ tile_start, int32_t* __restrict__ row_assign,
                        int32_t* __restrict__ row_token, float* __restrict__ row_weight,
-                       int32_t* dev_status, float4* __restrict__ zero, long long nzero4) {
+                       int32_t* __restrict__ assign_row, int32_t* dev_status,
+                       float4* __restrict__ zero, long long nzero4) {
   pdl_trigger();
   pdl_wait();  // y, the routing buffers and ids may belong to the previous kernel
   if (blockIdx.x > 0) {
@@ -229,6 +234,9 @@ __global__ void __launch_bounds__(1024)
       row_assign[r] = a;
       row_token[r] = a / k;
       row_weight[r] = __ldg(w + a);
+      assign_row[a] = r;
+    } else if (a < a1) {
+      assign_row[a] = -1;
     }
     __syncwarp();
   }
@@ -252,8 +260,8 @@ __global__ void __launch_bounds__(1024)
                       int32_t* __restrict__ end_offs, int32_t* __restrict__ start,
                       int32_t* __restrict__ tile_start, int32_t* __restrict__ row_assign,
                       int32_t* __restrict__ row_token, float* __restrict__ row_weight,
-                      int32_t* dev_status, int32_t* hist, int nb, float4* __restrict__ zero,
-                      long long nzero4) {
+                      int32_t* __restrict__ assign_row, int32_t* dev_status, int32_t* hist,
+                      int nb, float4* __restrict__ zero, long long nzero4) {
   pdl_trigger();
   pdl_wait();  // y, the routing buffers and ids may belong to the previous kernel
   cg::grid_group grid = cg::this_grid();
@@ -340,6 +348,9 @@ __global__ void __launch_bounds__(1024)
       row_assign[r] = a;
       row_token[r] = a / k;
       row_weight[r] = __ldg(w + a);
+      assign_row[a] = r;
+    } else if (a < a1) {
+      assign_row[a] = -1;
     }
     __syncwarp();
   }
@@ -409,34 +420,37 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
          (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
-// Backward operands in one pass over dy, one warp per padded row p of the
-// scaled, expert-sorted dY operand of dW:
-//   dyw[p]   = bf16(fl32(w_r * dy[token_r]))  for the sorted row r held in p,
-//              zeros in the padding rows of each expert's segment;
-//   dy_b[t]  = bf16(dy[t]), written by the row whose assignment is token t's
-//              first (a = t*k), so every token row is written exactly once;
+// Backward operands in one pass over dy, one warp per token t (each dy row
+// is read once):
+//   dy_b[t]  = bf16(dy[t]), the A operand of dX and of the d(routing weight)
+//              dots;
+//   dyw[p]   = bf16(fl32(w_a * dy[t]))  for each assignment a = t*k + j with
+//              a sorted row r = assign_row[a] (the padded row p = pstart[e]
+//              + r - start[e] of the expert e whose rows hold r): the scaled,
+//              expert-sorted dY operand of dW;
 //   dx[t] = 0 and dtopk[t*k .. t*k+k-1] = 0 (the dX GEMM accumulates into
-//   them), by the same row.
-// Every block derives the padded segment starts from the counts itself (a
-// block scan over at most 1024 experts) and keeps the expert tables in
-// shared memory, so the search for a row's expert costs no global round
-// trips; block 0 also publishes the padded starts and the dX tile prefix
-// sums (tiles of BM rows x tiles_n column blocks) for the GEMMs that
-// follow.  N % 8 == 0, K % 8 == 0.
+//   them).
+// Then one warp per padded row writes the zeros of the padding rows of each
+// expert's segment.  Every block derives the padded segment starts from the
+// counts itself (a block scan over at most 1024 experts) and keeps the
+// expert tables in shared memory, so a row's expert is found without global
+// round trips; block 0 also publishes the padded starts, the dX tile prefix
+// sums (tiles of BM rows x tiles_n column blocks) and the experts by
+// decreasing row count for the GEMMs that follow.  N % 8 == 0, K % 8 == 0.
 constexpr int kPrepThreads = 256;
+
 __global__ void __launch_bounds__(kPrepThreads)
-    bwd_prep_kernel(const float* __restrict__ dy, int N, int K, int k,
+    bwd_prep_kernel(const float* __restrict__ dy, int T, int N, int K, int k,
                     const int32_t* __restrict__ counts, const int32_t* __restrict__ start,
                     int BM, int tiles_n, int pad, int32_t* __restrict__ tile_start_dx,
-                    int32_t* __restrict__ pstart, const int32_t* __restrict__ row_token,
-                    const int32_t* __restrict__ row_assign,
+                    int32_t* __restrict__ pstart, const int32_t* __restrict__ assign_row,
                     const float* __restrict__ row_weight, int E, uint4* __restrict__ dyw,
                     uint4* __restrict__ dy_b, float4* __restrict__ dx, float* __restrict__ dtopk,
                     int32_t* __restrict__ expert_order) {
   pdl_trigger();
   pdl_wait();
   __shared__ int s_pstart[kMaxExperts + 1];
-  __shared__ int s_start[kMaxExperts];
+  __shared__ int s_start[kMaxExperts + 1];
   __shared__ int s_count[kMaxExperts];
   constexpr int PER = kMaxExperts / kPrepThreads;  // experts per thread in the scans
   {
@@ -468,6 +482,7 @@ __global__ void __launch_bounds__(kPrepThreads)
     }
     if (threadIdx.x == 0) {
       s_pstart[E] = ptot;
+      s_start[E] = __ldg(start + E);
       if (blockIdx.x == 0) {
         pstart[E] = ptot;
         tile_start_dx[E] = ttot;
@@ -489,55 +504,78 @@ __global__ void __launch_bounds__(kPrepThreads)
     if (threadIdx.x == 0) expert_order[E] = 0;
   }
   const int lane = threadIdx.x & 31;
-  const int wpb = blockDim.x >> 5;
-  const int total = s_pstart[E];
+  const int gwarp = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
   const int n8 = N / 8;
-  for (int p = blockIdx.x * wpb + (threadIdx.x >> 5); p < total; p += gridDim.x * wpb) {
-    int lo = 0, hi = E + 1;  // expert whose padded segment holds p
+  // the expert whose segment of `table` (E + 1 ascending starts) holds v
+  auto find = [&](const int* table, int v) {
+    int lo = 0, hi = E + 1;
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
-      if (s_pstart[mid] > p)
+      if (table[mid] > v)
         hi = mid;
       else
         lo = mid + 1;
     }
-    const int e = lo - 1;
-    const int local = p - s_pstart[e];
-    uint4* out = dyw + static_cast<size_t>(p) * n8;
-    if (local >= s_count[e]) {
-      for (int i = lane; i < n8; i += 32) out[i] = make_uint4(0, 0, 0, 0);
-      continue;
-    }
-    const int r = s_start[e] + local;
-    const float wr = __ldg(row_weight + r);
-    const int tok = __ldg(row_token + r);
-    const bool first = __ldg(row_assign + r) % k == 0;
-    const float4* src = reinterpret_cast<const float4*>(dy + static_cast<size_t>(tok) * N);
-    uint4* outb = dy_b + static_cast<size_t>(tok) * n8;
-#pragma unroll 4
-    for (int i = lane; i < n8; i += 32) {
-      const float4 a = __ldg(src + 2 * i);
-      const float4 b = __ldg(src + 2 * i + 1);
-      uint4 o;
-      o.x = pack_bf16x2(__fmul_rn(wr, a.x), __fmul_rn(wr, a.y));
-      o.y = pack_bf16x2(__fmul_rn(wr, a.z), __fmul_rn(wr, a.w));
-      o.z = pack_bf16x2(__fmul_rn(wr, b.x), __fmul_rn(wr, b.y));
-      o.w = pack_bf16x2(__fmul_rn(wr, b.z), __fmul_rn(wr, b.w));
-      out[i] = o;
-      if (first) {
-        uint4 q;
-        q.x = pack_bf16x2(a.x, a.y);
-        q.y = pack_bf16x2(a.z, a.w);
-        q.z = pack_bf16x2(b.x, b.y);
-        q.w = pack_bf16x2(b.z, b.w);
-        outb[i] = q;
+    return lo - 1;
+  };
+  for (int t = gwarp; t < T; t += nwarps) {
+    const float4* src = reinterpret_cast<const float4*>(dy + static_cast<size_t>(t) * N);
+    uint4* outb = dy_b + static_cast<size_t>(t) * n8;
+    // assignments j0 .. j0+31 of the token: lane j holds the padded row and
+    // weight of assignment j0 + j (p < 0: none)
+    for (int j0 = 0; j0 < k; j0 += 32) {
+      const int nj = min(32, k - j0);
+      int pj = -1;
+      float wj = 0.f;
+      if (lane < nj) {
+        const int r = __ldg(assign_row + static_cast<size_t>(t) * k + j0 + lane);
+        if (r >= 0) {
+          const int e = find(s_start, r);
+          pj = s_pstart[e] + (r - s_start[e]);
+          wj = __ldg(row_weight + r);
+        }
+      }
+      // uniform trip count: the shuffles below need the whole warp
+#pragma unroll 2
+      for (int i0 = 0; i0 < n8; i0 += 32) {
+        const int i = i0 + lane;
+        const bool act = i < n8;
+        const float4 a = act ? __ldg(src + 2 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 b = act ? __ldg(src + 2 * i + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j0 == 0 && act) {
+          uint4 q;
+          q.x = pack_bf16x2(a.x, a.y);
+          q.y = pack_bf16x2(a.z, a.w);
+          q.z = pack_bf16x2(b.x, b.y);
+          q.w = pack_bf16x2(b.z, b.w);
+          outb[i] = q;
+        }
+        for (int j = 0; j < nj; ++j) {
+          const int p = __shfl_sync(0xffffffffu, pj, j);
+          const float wr = __shfl_sync(0xffffffffu, wj, j);
+          if (p >= 0 && act) {
+            uint4 o;
+            o.x = pack_bf16x2(__fmul_rn(wr, a.x), __fmul_rn(wr, a.y));
+            o.y = pack_bf16x2(__fmul_rn(wr, a.z), __fmul_rn(wr, a.w));
+            o.z = pack_bf16x2(__fmul_rn(wr, b.x), __fmul_rn(wr, b.y));
+            o.w = pack_bf16x2(__fmul_rn(wr, b.z), __fmul_rn(wr, b.w));
+            dyw[static_cast<size_t>(p) * n8 + i] = o;
+          }
+        }
       }
     }
-    if (first) {
-      float4* dxr = dx + static_cast<size_t>(tok) * (K / 4);
-      for (int i = lane; i < K / 4; i += 32) dxr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j = lane; j < k; j += 32) dtopk[static_cast<size_t>(tok) * k + j] = 0.f;
-    }
+    float4* dxr = dx + static_cast<size_t>(t) * (K / 4);
+    for (int i = lane; i < K / 4; i += 32) dxr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = lane; j < k; j += 32) dtopk[static_cast<size_t>(t) * k + j] = 0.f;
+  }
+  // the padding rows of every expert's segment
+  const int total = s_pstart[E];
+  for (int p = gwarp; p < total; p += nwarps) {
+    const int e = find(s_pstart, p);
+    if (p - s_pstart[e] < s_count[e]) continue;
+    uint4* out = dyw + static_cast<size_t>(p) * n8;
+    for (int i = lane; i < n8; i += 32) out[i] = make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -574,8 +612,8 @@ size_t route_ws_bytes(int T, int k, int E) {
 cudaError_t launch_route(const int32_t* ids, const float* w, int T, int k, int E, int BM,
                          int tiles_n, int32_t* counts, int32_t* end_offs, int32_t* start,
                          int32_t* tile_start, int32_t* row_assign, int32_t* row_token,
-                         float* row_weight, int32_t* dev_status, void* ws, cudaStream_t st,
-                         float* zero, size_t zero_floats) {
+                         float* row_weight, int32_t* assign_row, int32_t* dev_status, void* ws,
+                         cudaStream_t st, float* zero, size_t zero_floats) {
   const int S = T * k;
   // the single-block router zeroes `zero` with its other blocks (float4 at a
   // time: needs 16-byte alignment and a multiple of 4 floats)
@@ -598,7 +636,7 @@ cudaError_t launch_route(const int32_t* ids, const float* w, int T, int k, int E
     cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(
         &cfg, route_coop_kernel, ids, w, S, k, E, BM, tiles_n, counts, end_offs, start, tile_start,
-        row_assign, row_token, row_weight, dev_status, static_cast<int32_t*>(ws), nb,
+        row_assign, row_token, row_weight, assign_row, dev_status, static_cast<int32_t*>(ws), nb,
         reinterpret_cast<float4*>(zero), fuse_zero ? static_cast<long long>(zero_floats / 4) : 0LL);
     if (e == cudaSuccess && zero && !fuse_zero && zero_floats > 0)
       e = cudaMemsetAsync(zero, 0, zero_floats * sizeof(float), st);
@@ -608,7 +646,7 @@ cudaError_t launch_route(const int32_t* ids, const float* w, int T, int k, int E
     const int blocks = 1 + (fuse_zero && zero_floats > 0 ? std::max(1, num_sms() - 1) : 0);
     cudaError_t e = launch_pdl(
         route_small_kernel, dim3(blocks), dim3(1024), 0, st, ids, w, S, k, E, BM, tiles_n, counts,
-        end_offs, start, tile_start, row_assign, row_token, row_weight, dev_status,
+        end_offs, start, tile_start, row_assign, row_token, row_weight, assign_row, dev_status,
         reinterpret_cast<float4*>(zero), fuse_zero ? static_cast<long long>(zero_floats / 4) : 0);
     if (e == cudaSuccess && zero && !fuse_zero && zero_floats > 0)
       e = cudaMemsetAsync(zero, 0, zero_floats * sizeof(float), st);
@@ -624,7 +662,7 @@ cudaError_t launch_route(const int32_t* ids, const float* w, int T, int k, int E
   route_scan_kernel<<<1, kScanThreads, 0, st>>>(chunk, nchunks, E, BM, tiles_n, counts,
                                                 end_offs, start, tile_start);
   route_scatter_kernel<<<nchunks, kRouteChunk, 0, st>>>(ids, w, S, k, E, chunk, row_assign,
-                                                        row_token, row_weight);
+                                                        row_token, row_weight, assign_row);
   return cudaGetLastError();
 }
 
@@ -642,17 +680,17 @@ cudaError_t launch_bwd_scan(const int32_t* counts, int E, int BM, int tiles_n, i
                     pad, tile_start_dx, pstart);
 }
 
-cudaError_t launch_bwd_prep(const float* dy, int N, int K, int k, const int32_t* counts,
+cudaError_t launch_bwd_prep(const float* dy, int T, int N, int K, int k, const int32_t* counts,
                             const int32_t* start, int BM, int tiles_n, int pad,
-                            int32_t* tile_start_dx, int32_t* pstart, const int32_t* row_token,
-                            const int32_t* row_assign, const float* row_weight, int E,
-                            int S_pad_max, void* dy_b, void* dyw, float* dx, float* dtopk,
-                            cudaStream_t st, int32_t* expert_order) {
+                            int32_t* tile_start_dx, int32_t* pstart, const int32_t* assign_row,
+                            const float* row_weight, int E, int S_pad_max, void* dy_b, void* dyw,
+                            float* dx, float* dtopk, cudaStream_t st, int32_t* expert_order) {
   const int wpb = kPrepThreads / 32;
-  const int blocks = std::max(1, std::min(cdiv(S_pad_max, wpb), num_sms() * (2048 / kPrepThreads)));
-  return launch_pdl(bwd_prep_kernel, dim3(blocks), dim3(kPrepThreads), 0, st, dy, N, K, k, counts,
-                    start, BM, tiles_n, pad, tile_start_dx, pstart, row_token, row_assign,
-                    row_weight, E, static_cast<uint4*>(dyw), static_cast<uint4*>(dy_b),
+  const int items = std::max(T, S_pad_max);
+  const int blocks = std::max(1, std::min(cdiv(items, wpb), num_sms() * (2048 / kPrepThreads)));
+  return launch_pdl(bwd_prep_kernel, dim3(blocks), dim3(kPrepThreads), 0, st, dy, T, N, K, k,
+                    counts, start, BM, tiles_n, pad, tile_start_dx, pstart, assign_row, row_weight,
+                    E, static_cast<uint4*>(dyw), static_cast<uint4*>(dy_b),
                     reinterpret_cast<float4*>(dx), dtopk,
                     expert_order && E <= kPrepThreads ? expert_order : nullptr);
 }

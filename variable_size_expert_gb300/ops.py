@@ -96,6 +96,7 @@ class RoutingBuffers:
     row_assign: torch.Tensor
     row_token: torch.Tensor
     row_weight: torch.Tensor
+    assign_row: torch.Tensor
 
     @staticmethod
     def empty(T: int, k: int, E: int, device) -> "RoutingBuffers":
@@ -105,7 +106,8 @@ class RoutingBuffers:
             counts=torch.empty(E, **i32), end_offs=torch.empty(E, **i32),
             start=torch.empty(E + 1, **i32), tile_start=torch.empty(E + 1, **i32),
             row_assign=torch.empty(S, **i32), row_token=torch.empty(S, **i32),
-            row_weight=torch.empty(S, dtype=torch.float32, device=device))
+            row_weight=torch.empty(S, dtype=torch.float32, device=device),
+            assign_row=torch.empty(S, **i32))
 
     def struct(self) -> L.Routing:
         return L.Routing(*(_ptr(getattr(self, f)) for f, _ in L.Routing._fields_))
