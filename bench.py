@@ -358,43 +358,86 @@ def sources_hash(names):
 
 
 def run_e2e(args, p, dev, lib, mgg, L, flops_step):
-    """Same metric through the public API from pinned host buffers: each step
-    copies its inputs host->device, runs forward + backward and copies every
-    result back device->host inside the timed region."""
+    """Same metric through the public API from pinned host buffers: every
+    step copies all its inputs host->device, runs forward + backward and
+    copies every result back device->host, all inside the timed region.
+    Steps are pipelined two deep on three streams (copies in, compute,
+    copies out, with two device buffer sets), so step i's results travel to
+    the host while step i+1 computes and step i+2's inputs arrive."""
     import torch
     T, K, N, E, k = p["T"], p["K"], p["N"], p["E"], p["k"]
-    host_in = {n: p[n].pin_memory() for n in ("x", "W", "expert_ids", "topk_weights", "dy")}
-    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host_in.items()}
-    host_out = {"y": torch.empty(T, N).pin_memory(), "dx": torch.empty(T, K).pin_memory(),
-                "dW": torch.empty(E, N, K).pin_memory(), "dtopk": torch.empty(T, k).pin_memory()}
-    routing = mgg.RoutingBuffers.empty(T, k, E, dev)
-    st = mgg.new_status(dev)
-
-    def step():
-        for n in host_in:
-            dev_in[n].copy_(host_in[n], non_blocking=True)
-        y, r = mgg.moe_forward(dev_in["x"], dev_in["W"], dev_in["expert_ids"], dev_in["topk_weights"],
-                               status=st, routing=routing)
-        dx, dW, dtopk = mgg.moe_backward(dev_in["dy"], dev_in["x"], dev_in["W"], r, k, status=st)
-        for n, t in (("y", y), ("dx", dx), ("dW", dW), ("dtopk", dtopk)):
-            host_out[n].copy_(t, non_blocking=True)
-
+    names_in = ("x", "W", "expert_ids", "topk_weights", "dy")
+    host_in = {n: p[n].pin_memory() for n in names_in}
+    shapes_out = {"y": (T, N), "dx": (T, K), "dW": (E, N, K), "dtopk": (T, k)}
+    host_out = [{n: torch.empty(sh).pin_memory() for n, sh in shapes_out.items()} for _ in range(2)]
+    sets = []
     for _ in range(2):
-        step()
+        sets.append({
+            "in": {n: torch.empty_like(t, device=dev) for n, t in host_in.items()},
+            "out": {n: torch.empty(sh, device=dev) for n, sh in shapes_out.items()},
+            "routing": mgg.RoutingBuffers.empty(T, k, E, dev),
+            "ws_f": torch.empty(mgg.workspace_bytes(L.MGG_OP_FORWARD, T, k, E, N, K),
+                                dtype=torch.uint8, device=dev),
+            "ws_b": torch.empty(mgg.workspace_bytes(L.MGG_OP_BACKWARD, T, k, E, N, K),
+                                dtype=torch.uint8, device=dev),
+            "loaded": torch.cuda.Event(), "computed": torch.cuda.Event(),
+            "drained": torch.cuda.Event()})
+    st = mgg.new_status(dev)
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    for b in sets:                       # the first use of each set waits on nothing
+        b["drained"].record(s_out)
+        b["computed"].record(s_cmp)
+
+    def step(i):
+        b = sets[i % 2]
+        ho = host_out[i % 2]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(b["computed"])   # step i-2 has read this set's inputs
+            for n in names_in:
+                b["in"][n].copy_(host_in[n], non_blocking=True)
+            b["loaded"].record(s_in)
+        with torch.cuda.stream(s_cmp):
+            s_cmp.wait_event(b["loaded"])
+            s_cmp.wait_event(b["drained"])  # step i-2's results have left this set
+            x, W, ids, w, dy = (b["in"][n] for n in names_in)
+            o = b["out"]
+            mgg.moe_forward(x, W, ids, w, status=st, out=o["y"], routing=b["routing"],
+                            workspace=b["ws_f"])
+            mgg.moe_backward(dy, x, W, b["routing"], k, status=st, dx=o["dx"], dW=o["dW"],
+                             dtopk=o["dtopk"], workspace=b["ws_b"])
+            b["computed"].record(s_cmp)
+        # (a second copy-out stream for half of dW measured no faster: the
+        # device->host path, about 170 GB/s here, is the limit)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(b["computed"])
+            for n in shapes_out:
+                ho[n].copy_(b["out"][n], non_blocking=True)
+            b["drained"].record(s_out)
+
+    for i in range(4):
+        step(i)
     torch.cuda.synchronize()
-    n = max(3, min(args.steps, 10))
+    n = max(4, min(args.steps, 12))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
     e0.record()
-    for _ in range(n):
-        step()
+    s_in.wait_stream(torch.cuda.current_stream())   # the timed copies start after e0
+    for i in range(n):
+        step(i)
+    for q in (s_in, s_cmp, s_out):
+        torch.cuda.current_stream().wait_stream(q)
     e1.record()
     torch.cuda.synchronize()
+    if mgg.read_status(st) != 0:
+        raise RuntimeError("device status set in the end-to-end run")
     ms = e0.elapsed_time(e1) / n
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
     return {"value": round(flops_step / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "note": "pinned host buffers; all inputs copied in and all outputs (y, dx, dW, dtopk) copied out each step"}
+            "note": ("pinned host buffers; all inputs (x, W, ids, weights, dy) copied in and all "
+                     "outputs (y, dx, dW, dtopk) copied out each step; steps pipelined two deep on "
+                     "three streams (copy in / compute / copy out)")}
 
 
 def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
