@@ -19,9 +19,9 @@
  *   allocates or frees device memory and never synchronises; everything is
  *   enqueued on `stream` (a cudaStream_t passed as void*, NULL = legacy
  *   default stream) in stream order, so every call can be captured in a
- *   CUDA graph.  (The bf16 backward forks onto one side stream per device,
- *   created with its two events on first use, and joins back; see
- *   mgg_moe_backward.)
+ *   CUDA graph.  (The bf16 backward forks onto a side stream, one per host
+ *   thread and device, created with its two events on first use, and joins
+ *   back; see mgg_moe_backward.)
  * - Layouts are dense row-major with the shapes given; no strides.
  * - "bf16" tensors hold IEEE bfloat16 bit patterns (uint16); "f32" tensors
  *   hold binary32.  Outputs are always f32 and are fully overwritten by the
@@ -265,8 +265,9 @@ mgg_status mgg_moe_forward(const void* x, const void* W, const int32_t* expert_i
  * T, k, E, N, K, dtype).
  * On the bf16 path the dX and dW GEMMs run side by side on disjoint sets of
  * the GPU's CTA pairs: the call forks onto a side stream the library creates
- * once per device (with two events) and joins back to `stream` before it
- * returns, so stream order and CUDA-graph capture hold as for any call.
+ * once per host thread and device (with two events) and joins back to
+ * `stream` before it returns, so stream order and CUDA-graph capture hold as
+ * for any call.
  * The environment variable MGG_BWD_SPLIT (a share of the pairs for dX in
  * (0, 1), or 0 for one after the other) overrides the split.
  */

@@ -121,3 +121,39 @@ def test_dw_dynamic_schedule_matches_static(T, K, N, E, k, routing, seed, monkey
         rdx, rdW, rdt = O.moe_backward(p["dy"].numpy(), f64(p["x"]), f64(p["W"]),
                                        p["expert_ids"].numpy(), p["topk_weights"].numpy())
         assert_bf16_close(dW_dyn, rdW, "dW dynamic")
+
+
+def test_backward_from_two_host_threads():
+    """Two host threads, each on its own stream, run backwards at once: the
+    side stream the bf16 backward forks onto is per thread, so neither waits
+    on (or races past) the other's events, and each gets the sequential
+    results."""
+    import threading
+    probs = [workloads.moe_problem(T=600, K=256, N=384, E=8, k=2, seed=s, routing="uniform",
+                                   with_dy=True) for s in (11, 12)]
+    refs = [_run_bwd(p) for p in probs]
+    outs = [None, None]
+
+    def work(i):
+        p = probs[i]
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            x, W = p["x"].to(DEV), p["W"].to(DEV)
+            ids, w, dy = p["expert_ids"].to(DEV), p["topk_weights"].to(DEV), p["dy"].to(DEV)
+            st = mgg.new_status(DEV)
+            _, r = mgg.moe_forward(x, W, ids, w, status=st)
+            res = None
+            for _ in range(5):
+                res = mgg.moe_backward(dy, x, W, r, k=2, status=st)
+            s.synchronize()
+            outs[i] = (res, mgg.read_status(st))
+
+    th = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    for (res, status), ref in zip(outs, refs):
+        assert status == 0
+        assert torch.equal(res[0], ref[0]) and torch.equal(res[1], ref[1])
+        torch.testing.assert_close(res[2], ref[2], rtol=1e-5, atol=1e-6)

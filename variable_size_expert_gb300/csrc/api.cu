@@ -85,25 +85,27 @@ int bwd_dx_pairs(int P, long long S, int E, int K, int N) {
   return best;
 }
 
-// One side stream and a fork/join event pair per device, created on first
-// use and kept (a fork onto it and a join back also capture into a graph).
+// One side stream and a fork/join event pair per host thread and device,
+// created on first use and kept (a fork onto it and a join back also capture
+// into a graph).  Per thread, so that calls from several host threads never
+// record or wait on one another's events.
 struct SideStream {
   cudaStream_t side;
   cudaEvent_t fork, join;
-  bool ok;
+  int state;  // 0 not created, 1 ready, -1 creation failed
 };
 SideStream* side_stream() {
-  static SideStream f[kMaxDevices];
-  static std::once_flag once[kMaxDevices];
+  thread_local SideStream f[kMaxDevices] = {};
   int dev = 0;
   if (!current_device(&dev)) return nullptr;
-  std::call_once(once[dev], [dev] {
-    SideStream& x = f[dev];
-    x.ok = cudaStreamCreateWithFlags(&x.side, cudaStreamNonBlocking) == cudaSuccess &&
-           cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) == cudaSuccess &&
-           cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) == cudaSuccess;
-  });
-  return f[dev].ok ? &f[dev] : nullptr;
+  SideStream& x = f[dev];
+  if (x.state == 0)
+    x.state = cudaStreamCreateWithFlags(&x.side, cudaStreamNonBlocking) == cudaSuccess &&
+                      cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) == cudaSuccess &&
+                      cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) == cudaSuccess
+                  ? 1
+                  : -1;
+  return x.state == 1 ? &x : nullptr;
 }
 
 // Benchmark instrumentation: event pairs recorded around the main GEMMs.
