@@ -452,7 +452,85 @@ def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
         else:
             os.environ["MGG_BWD_SPLIT"] = prev_split
     res["bwd_split"] = _bwd_split_extra(dev, mgg, flush)
+    res["dw_splitk"] = _dw_splitk_extra(dev, mgg, lib, flush)
     return res
+
+
+class _Env:
+    """Set (value str) or clear (None) environment variables for a block."""
+
+    def __init__(self, **kv):
+        self.kv = kv
+        self.prev = {}
+
+    def __enter__(self):
+        for n, v in self.kv.items():
+            self.prev[n] = os.environ.get(n)
+            if v is None:
+                os.environ.pop(n, None)
+            else:
+                os.environ[n] = v
+
+    def __exit__(self, *exc):
+        for n, v in self.prev.items():
+            if v is None:
+                os.environ.pop(n, None)
+            else:
+                os.environ[n] = v
+
+
+def _dw_splitk_extra(dev, mgg, lib, flush):
+    """dW with its contraction split across CTA pairs (planned per call from
+    the device counts) against unsplit (MGG_DW_SPLITK=0), on the two
+    workloads where a split is planned: fewer dW tiles than CTA pairs
+    (K = N = 512), and one hot expert holding half of the assignments
+    (K = N = 1024).  Per workload: the dW GEMM alone (dX and dW one after the
+    other, dW on every pair) and the whole backward call as it runs by
+    default (dX and dW side by side), both with and without the split."""
+    import torch
+    import workloads
+    out = {}
+    ev = Events(2)
+    h = ev.handles()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for name, c in (("narrow_K512_N512_E8_top2_T8192", workloads.BWD_NARROW),
+                    ("hot_expert_K1024_N1024_E8_top2", workloads.BWD_HOT)):
+        p = workloads.moe_problem(**c)
+        x, W, ids, w, dy = (p[n].to(dev) for n in ("x", "W", "expert_ids", "topk_weights", "dy"))
+        _, r = mgg.moe_forward(x, W, ids, w)
+        counts = r.counts.cpu().tolist()
+        k = ids.shape[1]
+        fl = 2.0 * c["T"] * k * c["K"] * c["N"]
+        row = {"counts": counts}
+        for tag, split in (("split", None), ("unsplit", "0")):
+            with _Env(MGG_DW_SPLITK=split, MGG_BWD_SPLIT="0"):
+                for _ in range(3):
+                    mgg.moe_backward(dy, x, W, r, k)
+                t_dw = []
+                for _ in range(10):
+                    flush.zero_()
+                    lib.mgg_set_kernel_events(h, 2)
+                    mgg.moe_backward(dy, x, W, r, k)
+                    lib.mgg_set_kernel_events(None, 0)
+                    torch.cuda.synchronize()
+                    t_dw.append(ev.ms(1))
+            with _Env(MGG_DW_SPLITK=split, MGG_BWD_SPLIT=None):
+                for _ in range(3):
+                    mgg.moe_backward(dy, x, W, r, k)
+                t_call = []
+                for _ in range(10):
+                    flush.zero_()
+                    s0.record()
+                    mgg.moe_backward(dy, x, W, r, k)
+                    s1.record()
+                    torch.cuda.synchronize()
+                    t_call.append(s0.elapsed_time(s1))
+            row[tag] = {"dw_gemm_us": round(statistics.median(t_dw) * 1e3, 2),
+                        "dw_gemm_tflops": round(fl / (statistics.median(t_dw) * 1e-3) / 1e12, 1),
+                        "backward_call_us": round(statistics.median(t_call) * 1e3, 2)}
+        out[name] = row
+        del x, W, ids, w, dy, r
+    return out
 
 
 def _bwd_split_extra(dev, mgg, flush):

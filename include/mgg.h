@@ -270,6 +270,17 @@ mgg_status mgg_moe_forward(const void* x, const void* W, const int32_t* expert_i
  * for any call.
  * The environment variable MGG_BWD_SPLIT (a share of the pairs for dX in
  * (0, 1), or 0 for one after the other) overrides the split.
+ * dW contraction split ("Grouped GEMM for MoE, in depth", §The backward
+ * pass: a hot expert's dW tiles have long contraction loops; split K across
+ * CTAs and reduce): where the dW tiles per expert (ceil(K/256) x ceil(N/256))
+ * are fewer than 0.8x the CTA pairs dW runs on (up to 256 experts), the
+ * call plans on the device, from the counts, a split of every expert whose
+ * contraction exceeds 1.25x the ideal per-pair load into the fewest pieces
+ * of at most that length (16 at most); the pieces add into that expert's dW,
+ * zeroed by the call.  An expert cut into three or more pieces gets a dW
+ * that is reproducible only to f32 rounding (the order of the additions
+ * varies); two pieces add onto zero in either order with the same bits.
+ * MGG_DW_SPLITK=0 turns the split off; MGG_DW_SPLITK=n caps the pieces at n.
  */
 mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
                             const mgg_routing* routing, int T, int K, int N, int E, int k,

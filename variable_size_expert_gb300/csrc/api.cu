@@ -51,13 +51,27 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
 mgg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MGG_OK : MGG_ERR_CUDA; }
 
+// Most pieces the dW contraction of one expert may be split into:
+// MGG_DW_SPLITK=0 (or 1) turns the split off, so dW is never accumulated
+// across CTA pairs.
+int dw_split_max() {
+  if (const char* s = getenv("MGG_DW_SPLITK")) {
+    const int v = atoi(s);
+    return v <= 1 ? 1 : std::min(v, kDwSplitMax);
+  }
+  return kDwSplitMax;
+}
+
 // CTA pairs the backward gives dX when it runs dX and dW side by side (the
 // rest go to dW); 0 runs them one after the other.  MGG_BWD_SPLIT overrides:
 // a share in (0, 1), or 0.  Otherwise the split balances the two GEMMs'
 // estimated makespans on P pairs: dX has about (S/256 + E/2) row blocks x
 // ceil(K/256) tiles of N/64 contraction steps, dW E x ceil(K/256) x
 // ceil(N/256) tiles of about S/E/64 steps, each dW step measured about 1.15x
-// a dX step (its output stores).
+// a dX step (its output stores).  (The estimate leaves out dW's contraction
+// split: counting it moved pairs from dX to dW at equal estimated cost and
+// made a K = N = 512 backward call slower, 63.9 -> 68.0 us; the prep still
+// splits for the pairs dW gets.)
 int bwd_dx_pairs(int P, long long S, int E, int K, int N) {
   if (const char* s = getenv("MGG_BWD_SPLIT")) {
     const double v = atof(s);
@@ -74,8 +88,7 @@ int bwd_dx_pairs(int P, long long S, int E, int K, int N) {
   double best_cost = 0.0;
   for (int a = 1; a < P; ++a) {
     const double dx = static_cast<double>((t_dx + a - 1) / a) * c_dx;
-    const double dw = std::max(static_cast<double>((t_dw + (P - a) - 1) / (P - a)),
-                               static_cast<double>(t_dw) / (P - a)) * c_dw;
+    const double dw = static_cast<double>((t_dw + (P - a) - 1) / (P - a)) * c_dw;
     const double cost = std::max(dx, dw);
     if (best == 0 || cost < best_cost) {
       best = a;
@@ -181,7 +194,7 @@ bool tmap_rows(CUtensorMap* m, const void* base, int rows, int cols, int box_row
 }
 
 struct BwdLayout {
-  size_t off_tile_start_dx, off_pstart, off_order, off_dy_b, off_dyw, total;
+  size_t off_tile_start_dx, off_pstart, off_order, off_dw_tiles, off_dy_b, off_dyw, total;
   int S_pad_max;
 };
 
@@ -195,6 +208,8 @@ BwdLayout bwd_layout(int T, int k, int E, int N, int K, mgg_dtype dt) {
   L.off_pstart = off;
   off += round256((E + 1) * sizeof(int32_t));
   L.off_order = off;  // E experts in dW's visiting order + dW's tile counter
+  off += round256((E + 1) * sizeof(int32_t));
+  L.off_dw_tiles = off;  // dW's tile prefix over the visiting order (split pieces included)
   off += round256((E + 1) * sizeof(int32_t));
   L.S_pad_max = 0;
   if (dt == MGG_BF16) {
@@ -562,15 +577,32 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
 
   void* dy_b = at<void>(ws, L.off_dy_b);
   void* dyw = at<void>(ws, L.off_dyw);
-  // expert visiting order of the dW GEMM (decreasing row count), for up to
-  // 256 experts; index order beyond
+  // expert visiting order of the dW GEMM (decreasing contraction), for up
+  // to 256 experts; index order beyond
   int32_t* order = E <= 256 ? at<int32_t>(ws, L.off_order) : nullptr;
+  // CTA pairs of the two backward GEMMs: dX and dW side by side on disjoint
+  // sets, or (0) one after the other on all
+  const int P = num_sms() / 2;
+  const int smax = dw_split_max();
+  const int pairs_dx = bwd_dx_pairs(P, static_cast<long long>(T) * k, E, K, N);
+  // dW's contraction split, planned by the prep from the device counts for
+  // the pairs dW gets (with the visiting order; none beyond 256 experts).
+  // A split needs an expert longer than 1.25x the per-pair load, which some
+  // expert's tiles alone exceed only if 5 tpe < 4 pairs; otherwise no plan
+  // is made and the dW GEMM decodes its tiles without reading one.
+  DwSplitPlan plan{};
+  plan.dW = dW;
+  plan.tpe = cdiv(K, kPairBM) * cdiv(N, kPairBN);
+  plan.pairs = pairs_dx > 0 ? P - pairs_dx : P;
+  plan.smax = smax;
+  const bool may_split = order && smax > 1 && 5LL * plan.tpe < 4LL * plan.pairs;
+  plan.tiles = may_split ? at<int32_t>(ws, L.off_dw_tiles) : nullptr;
   // one pass over dy: the backward schedules (dX tile prefix sums, padded
-  // segment starts), the bf16 operands of both GEMMs, and dx, dtopk zeroed
-  // for the dX epilogue's atomic adds
+  // segment starts, dW's order and split), the bf16 operands of both GEMMs,
+  // and dx, dtopk (and the split experts' dW) zeroed for the atomic adds
   if (launch_bwd_prep(dy, T, N, K, k, routing->counts, routing->start, BM, cdiv(K, BN), kDwPad,
                       tile_start_dx, pstart, routing->assign_row, routing->row_weight, E,
-                      L.S_pad_max, dy_b, dyw, dx, dtopk, st, order) != cudaSuccess)
+                      L.S_pad_max, dy_b, dyw, dx, dtopk, st, order, &plan) != cudaSuccess)
     return MGG_ERR_CUDA;
   p.A = dy_b;
   // dX reads W_e transposed: per stage each CTA takes 64 contraction rows of
@@ -583,6 +615,7 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   // dW's B operand, the scaled sorted dY [S_pad, N]: same choice over N.
   q.dyw = dyw;
   q.expert_order = order;
+  q.tile_prefix = plan.tiles;
   // dW's tile schedule: the static longest-first snake, or with
   // MGG_DW_SCHEDULE=dynamic a queue on the counter one past the order (reset
   // by the prep), measured slower on this GPU
@@ -614,8 +647,6 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
   auto dw_gemm = [&](cudaStream_t s) {
     return timed(1, s, [&] { return launch_dw_pair(tm_dyw, tm_dw, q, s); });
   };
-  const int P = num_sms() / 2;
-  const int pairs_dx = bwd_dx_pairs(P, static_cast<long long>(T) * k, E, K, N);
   if (pairs_dx <= 0) {
     if (dx_gemm(st) != cudaSuccess) return MGG_ERR_CUDA;
     return from_cuda(dw_gemm(st));

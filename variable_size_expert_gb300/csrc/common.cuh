@@ -135,6 +135,14 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// A load of data an earlier kernel may have written (ordinary, not through
+// the read-only path): as a volatile asm it stays after pdl_wait, where a
+// read-only (__ldg / const __restrict__) load may be scheduled before it.
+__device__ __forceinline__ int ld_dep(const int32_t* p) {
+  int v;
+  asm volatile("ld.global.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,

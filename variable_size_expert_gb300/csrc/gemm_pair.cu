@@ -617,25 +617,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
 
 // ====================================================================== dW
 struct DwTile {
-  int e, kbo, nb, m, nkb;
+  int e, kbo, nb, m;
+  int kb0;    // first contraction step of the tile's piece
+  int nkb;    // contraction steps of the piece
+  int split;  // the expert's contraction is split: the piece adds into dW
 };
 
-// Tile tau -> (expert, n block, k block): experts in the order given (the
-// backward prep ranks them by decreasing row count, so the static stride
-// hands out the longest contractions first and the last round holds the
-// shortest), n blocks, then k blocks fastest.
-__device__ __forceinline__ DwTile decode_dw(int tau, int tiles_k, int tiles_n,
+// Tile tau -> (expert, piece, n block, k block): experts in the order given
+// (the backward prep ranks them by decreasing piece length, so the static
+// stride hands out the longest contractions first and the last round holds
+// the shortest), the pieces of a split contraction, n blocks, then k blocks
+// fastest.  `prefix` (E+1, visiting order) holds each expert's first tile;
+// without it every expert has one piece.  Piece j of s covers the steps
+// [j nkb / s, (j+1) nkb / s) of the expert's nkb.
+// `prefix` is null when no expert is split (the kernel checks the total
+// once), so the common case keeps the closed-form decode.
+__device__ __forceinline__ DwTile decode_dw(int tau, int tiles_k, int tiles_n, int E,
                                             const int32_t* __restrict__ counts,
-                                            const int32_t* __restrict__ order) {
+                                            const int32_t* __restrict__ order,
+                                            const int32_t* __restrict__ prefix) {
   DwTile t;
   const int per = tiles_k * tiles_n;
-  const int eo = tau / per;
+  int eo, local, ns = 1, piece = 0;
+  if (prefix) {
+    int lo = 0, hi = E + 1;  // first i with prefix[i] > tau (every expert owns tiles)
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(prefix + mid) > tau)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    eo = lo - 1;
+    const int p0 = __ldg(prefix + eo);
+    ns = (__ldg(prefix + eo + 1) - p0) / per;
+    local = tau - p0;
+    piece = local / per;
+    local -= piece * per;
+  } else {
+    eo = tau / per;
+    local = tau - eo * per;
+  }
   t.e = order ? __ldg(order + eo) : eo;
-  const int local = tau - eo * per;
   t.nb = local / tiles_k;
   t.kbo = local - t.nb * tiles_k;
   t.m = __ldg(counts + t.e);
-  t.nkb = cdiv(t.m, BK);
+  const int steps = cdiv(t.m, BK);
+  t.split = ns > 1;
+  t.kb0 = t.split ? piece * steps / ns : 0;
+  t.nkb = t.split ? (piece + 1) * steps / ns - t.kb0 : steps;
   return t;
 }
 
@@ -645,7 +675,9 @@ __device__ __forceinline__ DwTile decode_dw(int tau, int tiles_k, int tiles_n,
 // the scaled, expert-sorted dY operand (MN-major, this CTA's 128 n-columns)
 // by TMA.  Rows past m_e are zero-filled on the x side and zero-padded on
 // the dY side.  Tiles of experts with no rows write zeros.
-template <bool DYN>
+// SPLIT: the experts' contractions may be split into pieces (the backward
+// prep's tile prefix is read); without it the tile decode is closed-form.
+template <bool DYN, bool SPLIT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : NUM_THREADS, 1)
     dw_pair_kernel(const __grid_constant__ CUtensorMap tmap_dyw,
                    const __grid_constant__ CUtensorMap tmap_dw, const DwParams p) {
@@ -676,9 +708,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
   const WaitCtl wc{m.abort_flag, p.dev_status, p.wait_limit};
   const int tiles_k = cdiv(p.K, PBM);
   const int tiles_n = cdiv(p.N, PBN);
-  const int total = p.E * tiles_k * tiles_n;
+  // tiles, split pieces included; the prefix is needed only if some expert is split
+  const int total =
+      SPLIT && p.tile_prefix ? ld_dep(p.tile_prefix + p.E) : p.E * tiles_k * tiles_n;
+  const int32_t* prefix = SPLIT && total != p.E * tiles_k * tiles_n ? p.tile_prefix : nullptr;
+  auto dw_tile = [&](int tau) {
+    return decode_dw(tau, tiles_k, tiles_n, p.E, p.counts, p.expert_order, prefix);
+  };
   // This pair's i-th tile.  The tiles are ordered by decreasing contraction
-  // (experts by row count); successive rounds of the persistent grid walk
+  // (experts by piece length); successive rounds of the persistent grid walk
   // the pairs in alternating directions (a snake), so each pair's sum of
   // long and short tiles stays close to the others'.  Increasing in i.
   auto snake = [&](int i) { return i * npairs + ((i & 1) ? npairs - 1 - pair : pair); };
@@ -692,7 +730,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
   if (dyn) {
     int live = 0;
     for (int e = 0; e < p.E; ++e) live += __ldg(p.counts + e) > 0;
-    live_tiles = live * tiles_k * tiles_n;
+    live_tiles = prefix ? __ldg(prefix + live) : live * tiles_k * tiles_n;
   }
   // i-th tile of this role's sequence from the ring (total at its end or on
   // a timeout).  A whole warp waits and reads; lane 0 (or the single
@@ -756,13 +794,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
     // row tokens of a stage are fetched two stages ahead of its copies, so
     // the dependent loads stay off the issue path.
     struct Cur {
-      int i, tau, kb, nkb, m, s0, k0;
+      int i, tau, kb, nkb, m, s0, k0, kb0;
     };
     auto seek = [&](Cur& cu) {
       while (cu.tau < total) {
-        const DwTile t = decode_dw(cu.tau, tiles_k, tiles_n, p.counts, p.expert_order);
+        const DwTile t = dw_tile(cu.tau);
         if (t.nkb > 0) {
           cu.nkb = t.nkb;
+          cu.kb0 = t.kb0;
           cu.m = t.m;
           cu.s0 = __ldg(p.start + t.e);
           cu.k0 = t.kbo * PBM + static_cast<int>(rank) * CBM;
@@ -781,11 +820,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
     auto load = [&](const Cur& cu, int(&tk)[4]) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int lr = cu.kb * BK + rr + 16 * i;
+        const int lr = (cu.kb0 + cu.kb) * BK + rr + 16 * i;
         tk[i] = cu.tau < total && lr < cu.m ? __ldg(p.row_token + cu.s0 + lr) : -1;
       }
     };
-    Cur cur{0, seq(0), 0, 1, 0, 0, 0};
+    Cur cur{0, seq(0), 0, 1, 0, 0, 0, 0};
     seek(cur);
     Cur pf = cur;
     int tk0[4], tk1[4], tk2[4];
@@ -844,7 +883,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
       int it = 0;
       bool ok = true;
       for (int i = 0, tau = seq1(0); ok && tau < total; tau = seq1(++i)) {
-        const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
+        const DwTile t = dw_tile(tau);
         const int ps = __ldg(p.pstart + t.e);
         const int n0 = t.nb * PBN + static_cast<int>(rank) * CBN;
         for (int kb = 0; kb < t.nkb; ++kb) {
@@ -858,12 +897,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
           const uint32_t dB = m.sB + s * B_STAGE;
           if (p.b_merged) {
             // both 64-wide chunks of this CTA's n columns in one box
-            tma_load_3d_cg2(dB, &tmap_dyw, full_l + 8 * s, 0, ps + kb * BK, n0 / 64);
+            tma_load_3d_cg2(dB, &tmap_dyw, full_l + 8 * s, 0, ps + (t.kb0 + kb) * BK, n0 / 64);
           } else {
 #pragma unroll
             for (int j = 0; j < CBN / 64; ++j)
               tma_load_2d_cg2(dB + j * CHUNK, &tmap_dyw, full_l + 8 * s, n0 + 64 * j,
-                              ps + kb * BK);
+                              ps + (t.kb0 + kb) * BK);
           }
           ++it;
         }
@@ -878,7 +917,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
       int it = 0;
       bool ok = true;
       for (int i = 0, tau = seq1(0); ok && tau < total; tau = seq1(++i)) {
-        const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
+        const DwTile t = dw_tile(tau);
         for (int kb = 0; kb < t.nkb; ++kb, ++it)
           if (!relay_stage<STAGES>(m, full_l, it, wc)) {
             ok = false;
@@ -891,7 +930,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
       int it = 0, tcount = 0;
       bool ok = true;
       for (int i = 0, tau = seq1(0); ok && tau < total; tau = seq1(++i)) {
-        const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
+        const DwTile t = dw_tile(tau);
         if (t.nkb == 0) continue;
         const int acc = tcount & 1;
         const uint32_t use = tcount >> 1;
@@ -947,7 +986,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
       return t;
     };
     for (int tau = enext(); tau < total; tau = enext()) {
-      const DwTile t = decode_dw(tau, tiles_k, tiles_n, p.counts, p.expert_order);
+      const DwTile t = dw_tile(tau);
       const int kw = t.kbo * PBM + static_cast<int>(rank) * CBM + warp * 32;  // warp's first k
       const int kcol = kw + lane;
       const int n0 = t.nb * PBN;
@@ -973,6 +1012,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
+        }
+        if (t.split) {
+          // one piece of a split contraction: every lane adds its column of
+          // the block into the zeroed dW (rows past N and columns past K
+          // skipped)
+          const int nb0 = n0 + cc * 32;
+          if (kcol < p.K) {
+            float* out = p.dW + (static_cast<size_t>(t.e) * p.N + nb0) * p.K + kcol;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (nb0 + i < p.N) atomicAdd(out + static_cast<size_t>(i) * p.K, v[i]);
+          }
+          continue;
         }
         const uint32_t buf = stg0 + (nst & 1) * DW_EPI_BUF;
         if (lane == 0) bulk_wait_read<1>();  // the store two blocks ago has read this buffer
@@ -1048,17 +1100,18 @@ cudaError_t launch_rows_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
   return launch_pdl(kern, dim3(grid), dim3(threads), smem, st, ta, tb, p);
 }
 
-template <bool DYN>
+template <bool DYN, bool SPLIT>
 cudaError_t launch_dw_pair_t(const CUtensorMap& tmap_dyw, const CUtensorMap& tmap_dw,
                              const DwParams& p, cudaStream_t st) {
   static bool done[64] = {};
   constexpr size_t smem = smem_bytes<kDwStages, kDwEpi>();
   constexpr int threads = DYN ? DW_THREADS : NUM_THREADS;
-  cudaError_t e = prepare(dw_pair_kernel<DYN>, smem, done);
+  auto kern = dw_pair_kernel<DYN, SPLIT>;
+  cudaError_t e = prepare(kern, smem, done);
   if (e != cudaSuccess) return e;
-  int grid = pair_grid(dw_pair_kernel<DYN>, smem, threads);
+  int grid = pair_grid(kern, smem, threads);
   if (p.max_pairs > 0) grid = std::min(grid, 2 * p.max_pairs);
-  return launch_pdl(dw_pair_kernel<DYN>, dim3(grid), dim3(threads), smem, st, tmap_dyw, tmap_dw, p);
+  return launch_pdl(kern, dim3(grid), dim3(threads), smem, st, tmap_dyw, tmap_dw, p);
 }
 
 }  // namespace
@@ -1088,8 +1141,10 @@ cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_
 
 cudaError_t launch_dw_pair(const CUtensorMap& tmap_dyw, const CUtensorMap& tmap_dw,
                            const DwParams& p, cudaStream_t st) {
-  if (p.tile_counter && p.expert_order) return launch_dw_pair_t<true>(tmap_dyw, tmap_dw, p, st);
-  return launch_dw_pair_t<false>(tmap_dyw, tmap_dw, p, st);
+  if (p.tile_counter && p.expert_order)
+    return launch_dw_pair_t<true, true>(tmap_dyw, tmap_dw, p, st);
+  if (p.tile_prefix) return launch_dw_pair_t<false, true>(tmap_dyw, tmap_dw, p, st);
+  return launch_dw_pair_t<false, false>(tmap_dyw, tmap_dw, p, st);
 }
 
 }  // namespace mgg

@@ -21,6 +21,30 @@ constexpr int kSimtBN = 64;    // f32 path tile columns
 constexpr int kRouteChunk = 256;
 constexpr int kMaxExperts = 1024;
 
+// Split of the dW contraction ("Grouped GEMM for MoE", §Backward: in dW a hot
+// expert has as many tiles as any other but longer contraction loops; the
+// remedy named there is to split the contraction across CTAs and reduce).
+// work = the contraction steps (kBK rows) summed over all dW tiles, pairs =
+// the CTA pairs the dW GEMM runs on.  The target piece length is the ideal
+// per-pair load (at least kDwSplitMin steps); an expert whose tiles are more
+// than 1.25x that long is cut into the fewest pieces of at most 1.25x the
+// target (at most kDwSplitMax, at most one per step), which add into a
+// zeroed dW.
+constexpr int kDwSplitMin = 16;  // 1024 rows; 8-step pieces measured no faster than whole tiles
+constexpr int kDwSplitMax = 16;
+
+__host__ __device__ inline long long dw_split_target(long long work, int pairs) {
+  const long long t = pairs > 0 ? (work + pairs - 1) / pairs : work;
+  return t > kDwSplitMin ? t : kDwSplitMin;
+}
+__host__ __device__ inline int dw_split_pieces(int steps, long long target, int smax) {
+  if (smax <= 1 || 4LL * steps <= 5LL * target) return 1;
+  long long s = (4LL * steps + 5LL * target - 1) / (5LL * target);
+  if (s > smax) s = smax;
+  if (s > steps) s = steps;
+  return s > 1 ? static_cast<int>(s) : 1;
+}
+
 // Default pipeline wait limit in SM clock cycles (about a second).
 constexpr long long kDefaultWaitLimit = 2000000000LL;
 
@@ -83,6 +107,9 @@ struct DwParams {
   int b_merged;                // tmap_dyw is the 3-D chunked view, one box per stage
   const int32_t* expert_order;  // [E] experts by decreasing row count (null: index order)
   int32_t* tile_counter;       // zeroed counter: dynamic tile queue (null: static schedule)
+  // [E+1] exclusive prefix of the tiles of the experts in visiting order,
+  // split pieces included (null: E x tiles per expert, no split)
+  const int32_t* tile_prefix;
   int max_pairs;               // cap on the persistent grid's CTA pairs (0: all that fit)
   int32_t* dev_status;
   long long wait_limit;
@@ -120,12 +147,22 @@ cudaError_t launch_offsets_scan(const int32_t* offs, bool is_sizes, int E, int r
                                 int32_t* dev_status, cudaStream_t st);
 cudaError_t launch_bwd_scan(const int32_t* counts, int E, int BM, int tiles_n, int pad,
                             int32_t* tile_start_dx, int32_t* pstart, cudaStream_t st);
+// What the backward prep needs to plan the dW contraction split: it writes
+// `tiles` (the dW tile prefix in visiting order, E+1 ints) and zeroes the
+// dW slices of the experts it splits.
+struct DwSplitPlan {
+  int32_t* tiles;   // [E+1]
+  float* dW;        // [E, N, K]
+  int tpe;          // dW tiles per expert and piece: ceil(K/256) x ceil(N/256)
+  int pairs;        // CTA pairs the dW GEMM runs on
+  int smax;         // most pieces per expert (1: no split)
+};
 cudaError_t launch_bwd_prep(const float* dy, int T, int N, int K, int k, const int32_t* counts,
                             const int32_t* start, int BM, int tiles_n, int pad,
                             int32_t* tile_start_dx, int32_t* pstart, const int32_t* assign_row,
                             const float* row_weight, int E, int S_pad_max, void* dy_b, void* dyw,
                             float* dx, float* dtopk, cudaStream_t st,
-                            int32_t* expert_order = nullptr);
+                            int32_t* expert_order = nullptr, const DwSplitPlan* split = nullptr);
 cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* start, int E, int BM,
                                   int max_tiles, int32_t* out, cudaStream_t st);
 

@@ -446,25 +446,37 @@ __global__ void __launch_bounds__(kPrepThreads)
                     int32_t* __restrict__ pstart, const int32_t* __restrict__ assign_row,
                     const float* __restrict__ row_weight, int E, uint4* __restrict__ dyw,
                     uint4* __restrict__ dy_b, float4* __restrict__ dx, float* __restrict__ dtopk,
-                    int32_t* __restrict__ expert_order) {
+                    int32_t* __restrict__ expert_order, DwSplitPlan split) {
   pdl_trigger();
   pdl_wait();
   __shared__ int s_pstart[kMaxExperts + 1];
   __shared__ int s_start[kMaxExperts + 1];
   __shared__ int s_count[kMaxExperts];
+  __shared__ int s_pieces[kMaxExperts];  // dW contraction pieces per expert
   constexpr int PER = kMaxExperts / kPrepThreads;  // experts per thread in the scans
   {
-    int cnt[PER], psum = 0, tsum = 0;
+    int cnt[PER], psum = 0, tsum = 0, wsum = 0;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int e = threadIdx.x * PER + i;
       cnt[i] = e < E ? __ldg(counts + e) : 0;
       psum += cdiv(cnt[i], pad) * pad;
       tsum += cdiv(cnt[i], BM) * tiles_n;
+      wsum += cdiv(cnt[i], kBK);
     }
-    int ptot, ttot;
+    int ptot, ttot, wtot;
     int prun = block_scan_excl(psum, 0, AddOp(), &ptot);
     int trun = block_scan_excl(tsum, 0, AddOp(), &ttot);
+    // every block plans the same dW split from the same counts
+    block_scan_excl(wsum, 0, AddOp(), &wtot);
+    const long long target =
+        dw_split_target(static_cast<long long>(wtot) * split.tpe, split.pairs);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = threadIdx.x * PER + i;
+      if (e < E)
+        s_pieces[e] = split.tiles ? dw_split_pieces(cdiv(cnt[i], kBK), target, split.smax) : 1;
+    }
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int e = threadIdx.x * PER + i;
@@ -491,17 +503,33 @@ __global__ void __launch_bounds__(kPrepThreads)
   }
   __syncthreads();
   if (expert_order && blockIdx.x == 0) {
-    // experts by decreasing row count, ties by index (E <= blockDim.x): the
-    // dW GEMM hands out the longest contractions first
+    // experts by decreasing dW piece length (contraction steps per piece),
+    // then decreasing row count, then index (E <= blockDim.x): the dW GEMM
+    // hands out the longest contractions first.  Without a split this is
+    // the order of decreasing row count.
+    __shared__ int s_otiles[kPrepThreads];
     const int e = threadIdx.x;
+    auto plen = [&](int f) { return cdiv(cdiv(s_count[f], kBK), s_pieces[f]); };
     if (e < E) {
-      const int c = s_count[e];
+      const int c = s_count[e], l = plen(e);
       int rank = 0;
-      for (int f = 0; f < E; ++f) rank += s_count[f] > c || (s_count[f] == c && f < e);
+      for (int f = 0; f < E; ++f) {
+        const int lf = plen(f);
+        rank += lf > l || (lf == l && (s_count[f] > c || (s_count[f] == c && f < e)));
+      }
       expert_order[rank] = e;
+      s_otiles[rank] = s_pieces[e] * split.tpe;
     }
     // one past the order: the dW GEMM's dynamic tile counter, reset here
     if (threadIdx.x == 0) expert_order[E] = 0;
+    __syncthreads();
+    if (split.tiles) {
+      // the dW tile prefix in visiting order (one expert per thread)
+      int tot;
+      const int ex = block_scan_excl(e < E ? s_otiles[e] : 0, 0, AddOp(), &tot);
+      if (e < E) split.tiles[e] = ex;
+      if (e == 0) split.tiles[E] = tot;
+    }
   }
   const int lane = threadIdx.x & 31;
   const int gwarp = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -576,6 +604,18 @@ __global__ void __launch_bounds__(kPrepThreads)
     if (p - s_pstart[e] < s_count[e]) continue;
     uint4* out = dyw + static_cast<size_t>(p) * n8;
     for (int i = lane; i < n8; i += 32) out[i] = make_uint4(0, 0, 0, 0);
+  }
+  // dW of the experts whose contraction is split: their pieces add into it
+  if (split.tiles) {
+    const size_t nk4 = static_cast<size_t>(N) * K / 4;
+    const size_t gt = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const size_t gn = static_cast<size_t>(gridDim.x) * blockDim.x;
+    float4* dW4 = reinterpret_cast<float4*>(split.dW);
+    for (int e = 0; e < E; ++e) {
+      if (s_pieces[e] <= 1) continue;
+      float4* o = dW4 + static_cast<size_t>(e) * nk4;
+      for (size_t i = gt; i < nk4; i += gn) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 }
 
@@ -684,15 +724,20 @@ cudaError_t launch_bwd_prep(const float* dy, int T, int N, int K, int k, const i
                             const int32_t* start, int BM, int tiles_n, int pad,
                             int32_t* tile_start_dx, int32_t* pstart, const int32_t* assign_row,
                             const float* row_weight, int E, int S_pad_max, void* dy_b, void* dyw,
-                            float* dx, float* dtopk, cudaStream_t st, int32_t* expert_order) {
+                            float* dx, float* dtopk, cudaStream_t st, int32_t* expert_order,
+                            const DwSplitPlan* split) {
   const int wpb = kPrepThreads / 32;
   const int items = std::max(T, S_pad_max);
   const int blocks = std::max(1, std::min(cdiv(items, wpb), num_sms() * (2048 / kPrepThreads)));
+  int32_t* order = expert_order && E <= kPrepThreads ? expert_order : nullptr;
+  // the split plan is published in visiting order, so it needs the order
+  DwSplitPlan sp{};
+  if (split && order && split->tiles && split->dW) sp = *split;
+  if (!sp.tiles) sp.tpe = 1;
   return launch_pdl(bwd_prep_kernel, dim3(blocks), dim3(kPrepThreads), 0, st, dy, T, N, K, k,
                     counts, start, BM, tiles_n, pad, tile_start_dx, pstart, assign_row, row_weight,
                     E, static_cast<uint4*>(dyw), static_cast<uint4*>(dy_b),
-                    reinterpret_cast<float4*>(dx), dtopk,
-                    expert_order && E <= kPrepThreads ? expert_order : nullptr);
+                    reinterpret_cast<float4*>(dx), dtopk, order, sp);
 }
 
 cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* start, int E, int BM,

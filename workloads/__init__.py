@@ -92,6 +92,16 @@ def _zipf_ids(rng, T, E, k, s):
     return ids
 
 
+def _hot_ids(rng, T, E, k):
+    # one hot expert: slot 0 of every token on expert 0, the other slots
+    # distinct experts drawn uniformly from 1..E-1
+    ids = np.zeros((T, k), dtype=np.int32)
+    if k > 1:
+        keys = rng.random((T, E - 1))
+        ids[:, 1:] = np.argsort(keys, axis=1, kind="stable")[:, :k - 1] + 1
+    return ids
+
+
 def _softmax_weights(rng, T, k):
     logits = rng.standard_normal((T, k))
     logits -= logits.max(axis=1, keepdims=True)
@@ -112,8 +122,9 @@ def moe_problem(T: int, K: int, N: int, E: int, k: int, seed: int = 0,
     routing: "uniform" (k distinct experts per token, uniformly), "zipf"
     (popularity ~ rank^-zipf_s over a seeded expert permutation, k distinct
     experts drawn without replacement), "random" (k independent uniform draws,
-    repeats allowed: the same expert twice is two assignments) or "given"
-    (use ``ids``).  weights: "uniform" U[0,1), "softmax" of N(0,1) logits, or
+    repeats allowed: the same expert twice is two assignments), "hot" (slot 0
+    of every token on expert 0, the other slots distinct and uniform over the
+    rest) or "given" (use ``ids``).  weights: "uniform" U[0,1), "softmax" of N(0,1) logits, or
     "pow2" (powers of two in {1, 1/2, 1/4, 1/8}, so that w*dy stays exactly
     representable in bfloat16 when dy is).
     """
@@ -126,6 +137,8 @@ def moe_problem(T: int, K: int, N: int, E: int, k: int, seed: int = 0,
         ids_ = _zipf_ids(rng, T, E, k, zipf_s)
     elif routing == "random":
         ids_ = rng.integers(0, E, size=(T, k), dtype=np.int32)
+    elif routing == "hot":
+        ids_ = _hot_ids(rng, T, E, k)
     elif routing == "given":
         ids_ = np.ascontiguousarray(ids, dtype=np.int32)
     else:
@@ -223,5 +236,11 @@ DECODE = dict(E=128, M_max=64, K=7168, N=2048, lam=8.0, seed=0)
 # the 1/64-scale copy of the backward workload used for finite differences
 BWD_SMALL = dict(T=64, K=32, N=32, E=8, k=2, seed=0, routing="uniform", weights="pow2",
                  with_dy=True)
+# dW with fewer tiles than CTA pairs (K = N = 512: 4 tiles per expert), and
+# with one hot expert holding half of the assignments (K = N = 1024)
+BWD_NARROW = dict(T=8192, K=512, N=512, E=8, k=2, seed=0, routing="uniform", weights="uniform",
+                  with_dy=True)
+BWD_HOT = dict(T=8192, K=1024, N=1024, E=8, k=2, seed=0, routing="hot", weights="uniform",
+               with_dy=True)
 # gated expert FFN, top-2: hidden 2048, FFN width 2048 (gate + up = 4096 columns)
 FFN_TOP2 = dict(T=4096, H=2048, F=2048, E=8, k=2, seed=0, routing="uniform", weights="uniform")
