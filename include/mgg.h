@@ -276,8 +276,9 @@ mgg_status mgg_moe_forward(const void* x, const void* W, const int32_t* expert_i
  * are fewer than 0.8x the CTA pairs dW runs on (up to 256 experts), the
  * call plans on the device, from the counts, a split of every expert whose
  * contraction exceeds 1.25x the ideal per-pair load into the fewest pieces
- * of at most that length (16 at most); the pieces add into that expert's dW,
- * zeroed by the call.  An expert cut into three or more pieces gets a dW
+ * of at most that length (16 at most; none when the whole tiles would run
+ * in one round of the pairs and the pieces would not); the pieces add into
+ * that expert's dW, zeroed by the call.  An expert cut into three or more pieces gets a dW
  * that is reproducible only to f32 rounding (the order of the additions
  * varies); two pieces add onto zero in either order with the same bits.
  * MGG_DW_SPLITK=0 turns the split off; MGG_DW_SPLITK=n caps the pieces at n.

@@ -40,6 +40,8 @@ def _expected_plan(counts, K, N, pairs, smax=16):
             return 1
         return max(1, min(math.ceil(4 * s / (5 * target)), smax, s))
     pc = [pieces(s) for s in steps]
+    if E * tpe <= pairs and sum(pc) * tpe > pairs:   # whole tiles in one round, pieces not
+        pc = [1] * E
     plen = [math.ceil(s / p) for s, p in zip(steps, pc)]
     order = sorted(range(E), key=lambda e: (-plen[e], -counts[e], e))
     prefix = [0]

@@ -439,6 +439,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // decreasing row count for the GEMMs that follow.  N % 8 == 0, K % 8 == 0.
 constexpr int kPrepThreads = 256;
 
+// With E experts cut into `pieces` in total: keep the dW split unless the
+// whole tiles fit in one round of the pairs and the pieces do not (then the
+// longest whole tile is the makespan either way).
+__device__ __forceinline__ bool dw_split_keep(int E, int pieces, int tpe, int pairs) {
+  return !(static_cast<long long>(E) * tpe <= pairs &&
+           static_cast<long long>(pieces) * tpe > pairs);
+}
+
 __global__ void __launch_bounds__(kPrepThreads)
     bwd_prep_kernel(const float* __restrict__ dy, int T, int N, int K, int k,
                     const int32_t* __restrict__ counts, const int32_t* __restrict__ start,
@@ -471,11 +479,23 @@ __global__ void __launch_bounds__(kPrepThreads)
     block_scan_excl(wsum, 0, AddOp(), &wtot);
     const long long target =
         dw_split_target(static_cast<long long>(wtot) * split.tpe, split.pairs);
+    int pc[PER], psum_pieces = 0;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int e = threadIdx.x * PER + i;
-      if (e < E)
-        s_pieces[e] = split.tiles ? dw_split_pieces(cdiv(cnt[i], kBK), target, split.smax) : 1;
+      pc[i] = e < E && split.tiles ? dw_split_pieces(cdiv(cnt[i], kBK), target, split.smax) : 1;
+      psum_pieces += e < E ? pc[i] : 0;
+    }
+    // When the whole tiles already run in one round (one per pair), the
+    // longest whole tile is the makespan: a split pays only if its pieces
+    // also fit in one round
+    int npieces;
+    block_scan_excl(psum_pieces, 0, AddOp(), &npieces);
+    const bool keep = dw_split_keep(E, npieces, split.tpe, split.pairs);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = threadIdx.x * PER + i;
+      if (e < E) s_pieces[e] = keep ? pc[i] : 1;
     }
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
