@@ -15,7 +15,8 @@ the pages it follows.  Page names used in citations:
   P3  "Grouped GEMM" (scholia-log, training-infra notes)
 
 Pins (what each function is checked against besides itself) live in
-``tests/test_oracle_pins.py``; every function here is pinned.
+``tests/test_oracle_pins.py``, ``tests/test_oracle_fp8_pins.py`` and
+``tests/test_oracle_ffn_backward_pins.py``; every function here is pinned.
 """
 from .mgg_oracle import *  # noqa: F401,F403
 from .mgg_oracle import __all__  # noqa: F401

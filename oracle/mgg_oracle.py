@@ -27,7 +27,8 @@ __all__ = [
     "bf16_round", "fp32_mul", "Routing", "route", "end_offsets", "tile_schedule",
     "schedule_stats", "grouped_gemm", "moe_forward", "moe_forward_unfused",
     "moe_backward", "moe_backward_rows", "moe_backward_dw_rows", "masked_grouped_gemm",
-    "moe_loss", "rel_frobenius", "max_abs_ratio", "silu", "moe_ffn_forward",
+    "moe_loss", "rel_frobenius", "max_abs_ratio", "silu", "moe_ffn_forward", "moe_ffn_backward",
+    "moe_ffn_loss",
     "E4M3_MAX", "e4m3_decode", "e4m3_encode", "quantize_fp8_rows", "grouped_gemm_fp8",
     "moe_forward_fp8", "masked_grouped_gemm_fp8",
 ]
@@ -378,6 +379,80 @@ def moe_ffn_forward(x, Wg, Wu, Wd, expert_ids, topk_weights, tokens=None, round_
             h[sel, j] = ha
             y[sel] += w[tok[sel], j][:, None] * (ha @ np.asarray(Wd[e], dtype=np.float64).T)
     return y, h
+
+
+def moe_ffn_backward(x, Wg, Wu, Wd, expert_ids, topk_weights, dy, bf16_operands=True):
+    """Gradients of L = sum(dy * y), y = moe_ffn_forward(x, Wg, Wu, Wd, ids, w).
+
+    Per assignment a = (t, j) of expert e, with g, u, h as in the forward and
+    s = sigmoid(g), silu(g) = g s:
+
+        a_dy = dy[t] Wd_e                         incoming gradient of h  [F]
+        dtopk[t, j] = <a_dy, h>                   (the unweighted product's gradient)
+        dh   = w[t, j] a_dy
+        dg   = dh * u * s * (1 + g (1 - s))       d silu(g) / dg = s (1 + g (1 - s))
+        du   = dh * silu(g)
+        dx[t]  += dg Wg_e + du Wu_e
+        dWg_e  += dg^T x[t],   dWu_e += du^T x[t]
+        dWd_e  += (w[t, j] dy[t])^T h
+
+    The forward's bfloat16 rounding of h is taken as the identity here (its
+    derivative is that of silu(g) u).  Each GEMM's operands are those of the
+    plain MoE backward: the down projection's backward reads bf16(dy) (dh,
+    dtopk) and bf16(fl32(w dy)) (dWd) with the bf16 h of the forward; the
+    gate/up backward reads dg and du rounded to bfloat16, as the tensor cores
+    consume them.  ``bf16_operands=False`` drops every rounding (h included):
+    the exact gradients of the float64 layer.
+
+    Returns (dx [T, H], dWg [E, F, H], dWu [E, F, H], dWd [E, H, F],
+    dtopk [T, k]).
+    """
+    ids = np.asarray(expert_ids)
+    w32 = np.asarray(topk_weights, dtype=np.float32)
+    x = np.asarray(x, dtype=np.float64)
+    dy32 = np.asarray(dy, dtype=np.float32)
+    rnd = bf16_round if bf16_operands else (lambda a: np.asarray(a, dtype=np.float64))
+    dyb = rnd(dy32)
+    T, H = x.shape
+    E, F = Wg.shape[0], Wg.shape[1]
+    k = ids.shape[1]
+    dx = np.zeros((T, H))
+    dWg = np.zeros((E, F, H))
+    dWu = np.zeros((E, F, H))
+    dWd = np.zeros((E, H, F))
+    dtopk = np.zeros((T, k))
+    for j in range(k):
+        for e in range(E):
+            t = np.nonzero(ids[:, j] == e)[0]
+            if t.size == 0:
+                continue
+            Wge = np.asarray(Wg[e], dtype=np.float64)
+            Wue = np.asarray(Wu[e], dtype=np.float64)
+            Wde = np.asarray(Wd[e], dtype=np.float64)
+            xt = x[t]
+            g = xt @ Wge.T
+            u = xt @ Wue.T
+            s = 1.0 / (1.0 + np.exp(-g))
+            sg = g * s
+            h = rnd(sg * u)
+            a_dy = dyb[t] @ Wde
+            dtopk[t, j] = np.sum(a_dy * h, axis=1)
+            dh = w32[t, j].astype(np.float64)[:, None] * a_dy
+            dg = rnd(dh * u * s * (1.0 + g * (1.0 - s)))
+            du = rnd(dh * sg)
+            dx[t] += dg @ Wge + du @ Wue
+            dWg[e] += dg.T @ xt
+            dWu[e] += du.T @ xt
+            dWd[e] += _dyw_operand(w32[t, j], dy32[t], bf16_operands).T @ h
+    return dx, dWg, dWu, dWd, dtopk
+
+
+def moe_ffn_loss(dy, x, Wg, Wu, Wd, expert_ids, topk_weights) -> float:
+    """L = sum(dy * y) of the float64 layer with h unrounded (the function
+    whose exact gradients ``moe_ffn_backward(..., bf16_operands=False)``
+    returns)."""
+    y, _ = moe_ffn_forward(x, Wg, Wu, Wd, expert_ids, topk_weights, round_h=False)
+    return moe_loss(dy, y)
 
 
 # --------------------------------------------------------------------------
