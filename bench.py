@@ -453,7 +453,69 @@ def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
             os.environ["MGG_BWD_SPLIT"] = prev_split
     res["bwd_split"] = _bwd_split_extra(dev, mgg, flush)
     res["dw_splitk"] = _dw_splitk_extra(dev, mgg, lib, flush)
+    res["ffn_backward"] = _ffn_backward_extra(dev, mgg, lib, flush)
     return res
+
+
+def _ffn_backward_extra(dev, mgg, lib, flush):
+    """Gated expert FFN training step pieces on the top-2 FFN workload
+    (T=4096, H=F=2048, E=8, k=2): the training forward (which also keeps g and
+    u) against the inference forward, and the backward call with the rate of
+    each of its GEMMs.  Useful FLOPs of the backward: dh 2SHF, dWd 2SHF, dx
+    4SHF (gate and up), dWg + dWu 4SHF: 12 S H F = 412.3 GFLOP."""
+    import torch
+    import workloads
+    c = workloads.FFN_BWD_TOP2
+    p = workloads.ffn_problem(**c)
+    T, H, F, E, k = c["T"], c["H"], c["F"], c["E"], c["k"]
+    S = T * k
+    d = {n: p[n].to(dev) for n in ("x", "Wg", "Wu", "Wd", "expert_ids", "topk_weights", "dy")}
+    fargs = [d[n] for n in ("x", "Wg", "Wu", "Wd", "expert_ids", "topk_weights")]
+    y = torch.empty(T, H, device=dev)
+    h = torch.empty(S, F, dtype=torch.bfloat16, device=dev)
+    gu = torch.empty(S, 2 * F, device=dev)
+    r = mgg.RoutingBuffers.empty(T, k, E, dev)
+    outs = dict(dx=torch.empty(T, H, device=dev), dWg=torch.empty(E, F, H, device=dev),
+                dWu=torch.empty(E, F, H, device=dev), dWd=torch.empty(E, H, F, device=dev),
+                dtopk=torch.empty(T, k, device=dev))
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed_call(fn, ev=None, nev=0):
+        for _ in range(3):
+            fn()
+        t, tk = [], []
+        for _ in range(10):
+            flush.zero_()
+            if ev is not None:
+                lib.mgg_set_kernel_events(ev.handles(), nev)
+            s0.record()
+            fn()
+            s1.record()
+            if ev is not None:
+                lib.mgg_set_kernel_events(None, 0)
+            torch.cuda.synchronize()
+            t.append(s0.elapsed_time(s1))
+            if ev is not None:
+                tk.append([ev.ms(i) for i in range(nev)])
+        return statistics.median(t), tk
+    t_inf, _ = timed_call(lambda: mgg.moe_ffn_forward(*fargs, out=y, h=h, routing=r))
+    t_trn, _ = timed_call(lambda: mgg.moe_ffn_forward(*fargs, out=y, h=h, routing=r, gu=gu))
+    ev = Events(6)
+    t_bwd, tk = timed_call(lambda: mgg.moe_ffn_backward(d["dy"], d["x"], d["Wg"], d["Wu"], d["Wd"],
+                                                        h, gu, r, k, **outs), ev, 6)
+    fl_unit = 2.0 * S * H * F
+    med = [statistics.median(x[i] for x in tk) for i in range(6)]
+    names = ("dh_swiglu_bwd", "dWd", "dx_gate", "dx_up", "dWg", "dWu")
+    return {
+        "workload": "gated FFN top-2: T=4096, H=F=2048, E=8, k=2, uniform routing, dy ~N(0,1); "
+                    "seed 0; L2 flushed",
+        "forward_inference_ms": round(t_inf, 4), "forward_training_ms": round(t_trn, 4),
+        "backward_ms": round(t_bwd, 4),
+        "backward_tflops": round(6 * fl_unit / (t_bwd * 1e-3) / 1e12, 1),
+        "backward_useful_gflop": round(6 * fl_unit / 1e9, 2),
+        "gemm_tflops": {n: round(fl_unit / (m * 1e-3) / 1e12, 1) for n, m in zip(names, med)},
+        "gemm_us": {n: round(m * 1e3, 1) for n, m in zip(names, med)},
+    }
 
 
 class _Env:

@@ -77,7 +77,8 @@ typedef enum {
   MGG_OP_BACKWARD = 2,
   MGG_OP_GROUPED_GEMM = 3,
   MGG_OP_MASKED = 4,
-  MGG_OP_FFN_FORWARD = 5
+  MGG_OP_FFN_FORWARD = 5,
+  MGG_OP_FFN_BACKWARD = 6
 } mgg_op;
 
 /* Bits the kernels OR into *dev_status. */
@@ -140,6 +141,7 @@ mgg_status mgg_tile_config(mgg_op op, mgg_dtype dtype, int* BM, int* BN, int* BK
  *   MGG_OP_GROUPED_GEMM          : E
  *   MGG_OP_MASKED                : 0 (no workspace)
  *   MGG_OP_FFN_FORWARD           : T, k, E (N = H, K = F unused)
+ *   MGG_OP_FFN_BACKWARD          : T, k, E, N = H, K = F, dtype (bf16)
  */
 size_t mgg_workspace_bytes(mgg_op op, int T, int k, int E, int N, int K, mgg_dtype dtype);
 
@@ -361,6 +363,10 @@ mgg_status mgg_moe_forward_fp8(const uint8_t* x, const float* x_scale, const uin
  *   h       [T*k, F] bf16, written: h[r] is the gated activation of sorted
  *           row r, i.e. of assignment routing->row_assign[r] (the operand a
  *           backward pass needs)
+ *   gu      [T*k, 2F] f32 or NULL: when given (a training forward), the gate
+ *           and up projections g = x[t] Wg_e^T (columns 0..F-1) and
+ *           u = x[t] Wu_e^T (columns F..2F-1) of sorted row r are written to
+ *           row r as well, for mgg_moe_ffn_backward
  *   routing filled as by mgg_route with N = H (its tile_start counts the
  *           down GEMM's tiles)
  * bf16 only (MGG_ERR_DTYPE otherwise); H % 8 == 0 and F % 8 == 0
@@ -371,8 +377,43 @@ mgg_status mgg_moe_forward_fp8(const uint8_t* x, const float* x_scale, const uin
 mgg_status mgg_moe_ffn_forward(const void* x, const void* Wg, const void* Wu, const void* Wd,
                                const int32_t* expert_ids, const float* topk_weights, int T,
                                int H, int F, int E, int k, mgg_dtype dtype, float* y, void* h,
-                               const mgg_routing* routing, int32_t* dev_status, void* ws,
-                               size_t ws_bytes, void* stream);
+                               float* gu, const mgg_routing* routing, int32_t* dev_status,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Gated expert FFN backward of L = sum(dy * y) for the layer of
+ * mgg_moe_ffn_forward ("Grouped GEMM for MoE, in depth", §The backward pass,
+ * for each of the layer's grouped GEMMs).  Per assignment a = (t, j) of
+ * expert e, sorted row r, with g, u from the forward, s = sigmoid(g):
+ *   a_dy       = bf16(dy[t]) Wd_e                               [F]
+ *   dtopk[t,j] = <a_dy, h[r]>          (h: the forward's bf16 h)
+ *   dh         = w[t,j] a_dy
+ *   dg = dh * u * s * (1 + g (1 - s)),  du = dh * g * s     (bf16 operands)
+ *   dx[t]     += dg Wg_e + du Wu_e                              [H]
+ *   dWg_e     += dg^T x[t],  dWu_e += du^T x[t]                 [F, H]
+ *   dWd_e     += bf16(fl32(w[t,j] dy[t]))^T h[r]                [H, F]
+ * (the forward's rounding of h to bf16 is taken as the identity).  Seven
+ * grouped GEMM launches after one pass over dy: dh with the SwiGLU backward
+ * in its epilogue (dy rows gathered by token, Wd read transposed), dWd (the
+ * dW GEMM over the sorted h rows), dx in two scatter GEMMs (dg | du rows,
+ * Wg and Wu read transposed, added into token rows) and dWg, dWu (the dW
+ * GEMM over x gathered by token).
+ *   dy [T, H] f32;  x, Wg, Wu, Wd as for the forward;  h [T*k, F] bf16 and
+ *   gu [T*k, 2F] f32 as the forward wrote them (gu required);  routing the
+ *   forward's.
+ *   dx [T, H], dWg, dWu [E, F, H], dWd [E, H, F], dtopk [T, k]: f32,
+ *   overwritten (an expert with no rows gets exact +0 weight gradients).
+ * bf16 only; H % 8 == 0 and F % 8 == 0; 16-byte aligned pointers (dtopk 4).
+ * ws: mgg_workspace_bytes(MGG_OP_FFN_BACKWARD, T, k, E, H, F, MGG_BF16).
+ * Results are reproducible to f32 rounding: dx, dtopk and the token-row
+ * additions of the two dx GEMMs are atomic adds.
+ */
+mgg_status mgg_moe_ffn_backward(const float* dy, const void* x, const void* Wg, const void* Wu,
+                                const void* Wd, const void* h, const float* gu,
+                                const mgg_routing* routing, int T, int H, int F, int E, int k,
+                                mgg_dtype dtype, float* dx, float* dWg, float* dWu, float* dWd,
+                                float* dtopk, int32_t* dev_status, void* ws, size_t ws_bytes,
+                                void* stream);
 
 /*
  * Debug export of the device tile schedule: for every tile index tau of the

@@ -132,6 +132,34 @@ def test_fp8_invalid_arguments_rejected_before_launch(lib):
                                 1 << 20, None) == L.MGG_ERR_DTYPE
 
 
+def test_ffn_backward_invalid_arguments_rejected_before_launch(lib):
+    from variable_size_expert_gb300 import _lib as L
+    fake = ctypes.c_void_p(0x10000)        # never dereferenced: checks fail first
+    r = L.Routing(*([0x10000] * 8))
+    ws = L.MGG_OP_FFN_BACKWARD
+    need = lib.mgg_workspace_bytes(ws, 4096, 2, 8, 2048, 2048, L.MGG_BF16)
+    # the plain backward's tables and operands over H, then dg | du [S, 2F]
+    # bf16 and the identity map and unit weights [S]
+    assert need >= lib.mgg_workspace_bytes(L.MGG_OP_BACKWARD, 4096, 2, 8, 2048, 2048, L.MGG_BF16) \
+        + 8192 * 4096 * 2 + 2 * 8192 * 4
+    assert lib.mgg_workspace_bytes(ws, 64, 2, 8, 64, 64, L.MGG_F32) == 0       # bf16 only
+
+    def call(dy=fake, gu=fake, F=64, dtype=L.MGG_BF16, dWd=fake, wsb=1 << 30, x=fake):
+        return lib.mgg_moe_ffn_backward(dy, x, fake, fake, fake, fake, gu, ctypes.byref(r), 4, 64,
+                                        F, 2, 1, dtype, fake, fake, fake, dWd, fake, fake, fake,
+                                        wsb, None)
+    assert call(gu=None) == L.MGG_ERR_INVALID_ARG           # the forward's g, u are required
+    assert call(dWd=None) == L.MGG_ERR_INVALID_ARG
+    assert call(dtype=L.MGG_F32) == L.MGG_ERR_DTYPE
+    assert call(F=60) == L.MGG_ERR_ALIGNMENT
+    assert call(x=ctypes.c_void_p(0x10008)) == L.MGG_ERR_ALIGNMENT
+    assert call(wsb=64) == L.MGG_ERR_WORKSPACE
+    # the forward's optional gu must be 16-byte aligned when given
+    assert lib.mgg_moe_ffn_forward(fake, fake, fake, fake, fake, fake, 4, 64, 64, 2, 1, L.MGG_BF16,
+                                   fake, fake, ctypes.c_void_p(0x10004), ctypes.byref(r), fake,
+                                   fake, 1 << 30, None) == L.MGG_ERR_ALIGNMENT
+
+
 def test_product_path_has_no_oracle_or_fallback():
     """The package never imports the oracle, and fails loudly without its library."""
     pkg = os.path.join(ROOT, "variable_size_expert_gb300")

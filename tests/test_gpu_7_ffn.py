@@ -116,7 +116,8 @@ def test_ffn_errors():
     def call(F=64, dtype=L.MGG_BF16, nbytes=ws.numel()):
         return lib.mgg_moe_ffn_forward(x.data_ptr(), Wg.data_ptr(), Wu.data_ptr(), Wd.data_ptr(),
                                        ids.data_ptr(), w.data_ptr(), 8, 64, F, 2, 1, dtype,
-                                       y.data_ptr(), h.data_ptr(), ctypes.byref(rs), st.data_ptr(),
+                                       y.data_ptr(), h.data_ptr(), None, ctypes.byref(rs),
+                                       st.data_ptr(),
                                        ws.data_ptr(), nbytes, torch.cuda.current_stream().cuda_stream)
     assert call(dtype=L.MGG_F32) == L.MGG_ERR_DTYPE
     assert call(F=60) == L.MGG_ERR_ALIGNMENT

@@ -34,6 +34,7 @@ MGG_OP_BACKWARD = 2
 MGG_OP_GROUPED_GEMM = 3
 MGG_OP_MASKED = 4
 MGG_OP_FFN_FORWARD = 5
+MGG_OP_FFN_BACKWARD = 6
 # device status bits
 MGG_DEV_BAD_EXPERT_ID = 0x1
 MGG_DEV_BAD_OFFSETS = 0x2
@@ -46,7 +47,7 @@ EXPORTS = (
     "mgg_status_string", "mgg_tile_config", "mgg_workspace_bytes", "mgg_route",
     "mgg_grouped_gemm", "mgg_moe_forward", "mgg_moe_backward", "mgg_debug_tile_schedule",
     "mgg_set_kernel_events", "mgg_route_noalloc", "mgg_moe_ffn_forward", "mgg_quantize_fp8",
-    "mgg_grouped_gemm_fp8", "mgg_moe_forward_fp8",
+    "mgg_grouped_gemm_fp8", "mgg_moe_forward_fp8", "mgg_moe_ffn_backward",
 )
 
 
@@ -79,8 +80,10 @@ _SIGS = {
     "mgg_debug_tile_schedule": (_I, [_RP, _I, _I, _I, _I, _P, _P]),
     "mgg_set_kernel_events": (_I, [ctypes.POINTER(_P), _I]),
     "mgg_route_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _RP, _P, _P]),
-    "mgg_moe_ffn_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _RP, _P,
-                                 _P, _SZ, _P]),
+    "mgg_moe_ffn_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _RP,
+                                 _P, _P, _SZ, _P]),
+    "mgg_moe_ffn_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _RP, _I, _I, _I, _I, _I, _I, _P, _P,
+                                  _P, _P, _P, _P, _P, _SZ, _P]),
     "mgg_quantize_fp8": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "mgg_grouped_gemm_fp8": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "mgg_moe_forward_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _RP, _P, _P, _SZ,

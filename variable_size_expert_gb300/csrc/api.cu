@@ -223,6 +223,30 @@ BwdLayout bwd_layout(int T, int k, int E, int N, int K, mgg_dtype dt) {
   return L;
 }
 
+// Gated FFN backward workspace (H = N, F = K): the plain backward's layout
+// over the down projection (its dX tile prefix counts the tiles of the
+// SwiGLU-backward GEMM over F), then dg | du (bf16 [S, 2F], sorted rows), the
+// identity row map and unit weights [S].
+struct FfnBwdLayout {
+  BwdLayout b;
+  size_t off_dgu, off_iota, off_ones, total;
+};
+
+FfnBwdLayout ffn_bwd_layout(int T, int k, int E, int H, int F) {
+  FfnBwdLayout L{};
+  L.b = bwd_layout(T, k, E, H, H, MGG_BF16);
+  const size_t S = static_cast<size_t>(T) * k;
+  size_t off = L.b.total;
+  L.off_dgu = off;
+  off += round256(S * 2 * F * 2);
+  L.off_iota = off;
+  off += round256(S * 4);
+  L.off_ones = off;
+  off += round256(S * 4);
+  L.total = off;
+  return L;
+}
+
 template <typename T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
@@ -366,6 +390,10 @@ size_t mgg_workspace_bytes(mgg_op op, int T, int k, int E, int N, int K, mgg_dty
     case MGG_OP_FFN_FORWARD:
       if (T < 1 || k < 1 || E < 1 || E > kMaxExperts) return 0;
       return route_ws_bytes(T, k, E) + 2 * round256((E + 1) * sizeof(int32_t));
+    case MGG_OP_FFN_BACKWARD:
+      if (T < 1 || k < 1 || E < 1 || E > kMaxExperts || N < 1 || K < 1) return 0;
+      if (dtype != MGG_BF16) return 0;
+      return ffn_bwd_layout(T, k, E, N, K).total;
   }
   return 0;
 }
@@ -796,8 +824,8 @@ mgg_status mgg_moe_forward_fp8(const uint8_t* x, const float* x_scale, const uin
 mgg_status mgg_moe_ffn_forward(const void* x, const void* Wg, const void* Wu, const void* Wd,
                                const int32_t* expert_ids, const float* topk_weights, int T,
                                int H, int F, int E, int k, mgg_dtype dtype, float* y, void* h,
-                               const mgg_routing* routing, int32_t* dev_status, void* ws,
-                               size_t ws_bytes, void* stream) {
+                               float* gu, const mgg_routing* routing, int32_t* dev_status,
+                               void* ws, size_t ws_bytes, void* stream) {
   if (!x || !Wg || !Wu || !Wd || !expert_ids || !topk_weights || !y || !h ||
       !routing_ok(routing) || !dev_status || !ws)
     return MGG_ERR_INVALID_ARG;
@@ -807,7 +835,7 @@ mgg_status mgg_moe_ffn_forward(const void* x, const void* Wg, const void* Wu, co
   if (F < 1) return MGG_ERR_INVALID_ARG;
   if (F % 8 != 0) return MGG_ERR_ALIGNMENT;
   if (!aligned(x, 16) || !aligned(Wg, 16) || !aligned(Wu, 16) || !aligned(Wd, 16) ||
-      !aligned(y, 16) || !aligned(h, 16))
+      !aligned(y, 16) || !aligned(h, 16) || !aligned(gu, 16))
     return MGG_ERR_ALIGNMENT;
   if (ws_bytes < mgg_workspace_bytes(MGG_OP_FFN_FORWARD, T, k, E, H, F, dtype) || !aligned(ws, 256))
     return MGG_ERR_WORKSPACE;
@@ -840,13 +868,16 @@ mgg_status mgg_moe_ffn_forward(const void* x, const void* Wg, const void* Wu, co
   p.Nout = F;
   p.hout = h;
   p.ldh = F;
+  p.guout = gu;  // the training forward also keeps g and u for the backward
+  p.ldgu = 2 * F;
   p.dev_status = dev_status;
   p.wait_limit = wait_limit();
   CUtensorMap tg, tu;
   if (!tmap_weights(&tg, Wg, E, F, H, kBK, kPairBN / 2) ||
       !tmap_weights(&tu, Wu, E, F, H, kBK, kPairBN / 2))
     return MGG_ERR_CUDA;
-  if (timed(0, st, [&] { return launch_rows_pair(kModeGateUp, false, tu, tg, p, st); }) !=
+  const int gu_mode = gu ? kModeGateUpSave : kModeGateUp;
+  if (timed(0, st, [&] { return launch_rows_pair(gu_mode, false, tu, tg, p, st); }) !=
       cudaSuccess)
     return MGG_ERR_CUDA;
   // down projection: h rows in sorted order by TMA, scatter-combine into y
@@ -867,6 +898,153 @@ mgg_status mgg_moe_ffn_forward(const void* x, const void* Wg, const void* Wu, co
   if (!tmap_rows(&th, h, T * k, F, kPairBM / 2) || !tmap_weights(&td, Wd, E, H, F, kBK, kPairBN / 2))
     return MGG_ERR_CUDA;
   return from_cuda(timed(1, st, [&] { return launch_rows_pair(kModeScatter, false, th, td, q, st); }));
+}
+
+mgg_status mgg_moe_ffn_backward(const float* dy, const void* x, const void* Wg, const void* Wu,
+                                const void* Wd, const void* h, const float* gu,
+                                const mgg_routing* routing, int T, int H, int F, int E, int k,
+                                mgg_dtype dtype, float* dx, float* dWg, float* dWu, float* dWd,
+                                float* dtopk, int32_t* dev_status, void* ws, size_t ws_bytes,
+                                void* stream) {
+  if (!dy || !x || !Wg || !Wu || !Wd || !h || !gu || !routing_ok(routing) || !dx || !dWg ||
+      !dWu || !dWd || !dtopk || !dev_status || !ws)
+    return MGG_ERR_INVALID_ARG;
+  if (dtype != MGG_BF16) return MGG_ERR_DTYPE;
+  mgg_status s = check_moe_sizes(T, H, H, E, k, dtype);
+  if (s != MGG_OK) return s;
+  if (F < 1) return MGG_ERR_INVALID_ARG;
+  if (F % 8 != 0) return MGG_ERR_ALIGNMENT;
+  if (!aligned(dy, 16) || !aligned(x, 16) || !aligned(Wg, 16) || !aligned(Wu, 16) ||
+      !aligned(Wd, 16) || !aligned(h, 16) || !aligned(gu, 16) || !aligned(dx, 16) ||
+      !aligned(dWg, 16) || !aligned(dWu, 16) || !aligned(dWd, 16) || !aligned(dtopk, 4))
+    return MGG_ERR_ALIGNMENT;
+  const FfnBwdLayout L = ffn_bwd_layout(T, k, E, H, F);
+  if (ws_bytes < L.total || !aligned(ws, 256)) return MGG_ERR_WORKSPACE;
+  s = check_arch();
+  if (s != MGG_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int S = T * k;
+  int32_t* tile_start_dh = at<int32_t>(ws, L.b.off_tile_start_dx);
+  int32_t* pstart = at<int32_t>(ws, L.b.off_pstart);
+  int32_t* order = E <= 256 ? at<int32_t>(ws, L.b.off_order) : nullptr;
+  void* dy_b = at<void>(ws, L.b.off_dy_b);
+  void* dyw = at<void>(ws, L.b.off_dyw);
+  __nv_bfloat16* dgu = at<__nv_bfloat16>(ws, L.off_dgu);
+  int32_t* iota = at<int32_t>(ws, L.off_iota);
+  float* ones = at<float>(ws, L.off_ones);
+  if (launch_iota_ones(iota, ones, S, st) != cudaSuccess) return MGG_ERR_CUDA;
+  // one pass over dy: bf16(dy) for dh and d(routing weight), the scaled
+  // sorted bf16(fl32(w dy)) for dWd, the SwiGLU-backward GEMM's tile prefix
+  // (over F), dx and dtopk zeroed for the atomic adds
+  if (launch_bwd_prep(dy, T, H, H, k, routing->counts, routing->start, kPairBM, cdiv(F, kPairBN),
+                      kDwPad, tile_start_dh, pstart, routing->assign_row, routing->row_weight, E,
+                      L.b.S_pad_max, dy_b, dyw, dx, dtopk, st, order) != cudaSuccess)
+    return MGG_ERR_CUDA;
+
+  // dh = w (bf16(dy) Wd_e), with the d(routing weight) dot against the
+  // forward's h, then dg | du from the saved g, u: the dX GEMM's main loop
+  // (dy rows gathered by token, Wd read transposed) with the gated epilogue
+  RowsParams p{};
+  p.A = dy_b;
+  p.lda = H;
+  p.Kc = H;
+  p.row_token = routing->row_token;
+  p.row_weight = routing->row_weight;
+  p.row_assign = routing->row_assign;
+  p.tile_start = tile_start_dh;
+  p.start = routing->start;
+  p.E = E;
+  p.Nout = F;
+  p.xdot = h;
+  p.ldx = F;
+  p.dtopk = dtopk;
+  p.gu = gu;
+  p.ldgu = 2 * F;
+  p.hout = dgu;
+  p.ldh = 2 * F;
+  p.dev_status = dev_status;
+  p.wait_limit = wait_limit();
+  CUtensorMap tm_wd;
+  p.b_merged = F % 64 == 0 && tmap_weights_chunked(&tm_wd, Wd, E, H, F);
+  if (!p.b_merged && !tmap_weights(&tm_wd, Wd, E, H, F, 64, 64)) return MGG_ERR_CUDA;
+  if (timed(0, st, [&] { return launch_rows_pair(kModeSwiGluBwd, true, tm_wd, tm_wd, p, st); }) !=
+      cudaSuccess)
+    return MGG_ERR_CUDA;
+
+  // dW GEMMs over a [rows, N] bf16 operand b (row stride ld) for the
+  // experts' rows starting at bstart: dWd over h (identity row map) and the
+  // scaled dy; dWg, dWu over x (gathered by token) and the dg, du halves
+  auto dw_gemm = [&](int slot, const void* a, const int32_t* a_rows, int Ka, const void* b,
+                     int rows, int N, int ld, const int32_t* bstart, float* out) -> bool {
+    DwParams q{};
+    q.x = a;
+    q.K = Ka;
+    q.N = N;
+    q.counts = routing->counts;
+    q.start = routing->start;
+    q.pstart = bstart;
+    q.row_token = a_rows;
+    q.row_weight = routing->row_weight;
+    q.E = E;
+    q.dW = out;
+    q.expert_order = order;
+    q.dev_status = dev_status;
+    q.wait_limit = wait_limit();
+    CUtensorMap tb, to;
+    q.b_merged = 0;
+    if (N % 64 == 0) {
+      const uint64_t dims[3] = {64, static_cast<uint64_t>(rows), static_cast<uint64_t>(N / 64)};
+      const uint64_t strides[2] = {static_cast<uint64_t>(ld) * 2, 128};
+      const uint32_t box[3] = {64, static_cast<uint32_t>(kDwPad), 2};
+      q.b_merged = encode_tmap(&tb, b, 3, dims, strides, box);
+    }
+    if (!q.b_merged) {
+      const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(rows)};
+      const uint64_t strides[1] = {static_cast<uint64_t>(ld) * 2};
+      const uint32_t box[2] = {64, static_cast<uint32_t>(kDwPad)};
+      if (!encode_tmap(&tb, b, 2, dims, strides, box)) return false;
+    }
+    if (!tmap_dw_store(&to, out, E, N, Ka)) return false;
+    return timed(slot, st, [&] { return launch_dw_pair(tb, to, q, st); }) == cudaSuccess;
+  };
+  // dWd_e = sum (w dy)^T h: the padded scaled dy rows (prep) against h
+  if (!dw_gemm(1, h, iota, F, dyw, L.b.S_pad_max, H, H, pstart, dWd)) return MGG_ERR_CUDA;
+
+  // dx[t] += dg Wg_e and du Wu_e: dg | du rows by TMA (sorted order), the
+  // weights read transposed, unit row weights, added into the token rows
+  for (int half = 0; half < 2; ++half) {
+    RowsParams r{};
+    r.Kc = F;
+    r.lda = 2 * F;
+    r.row_token = routing->row_token;
+    r.row_weight = ones;
+    r.tile_start = routing->tile_start;
+    r.start = routing->start;
+    r.E = E;
+    r.Nout = H;
+    r.out = dx;
+    r.ldo = H;
+    r.dev_status = dev_status;
+    r.wait_limit = wait_limit();
+    const void* Wh = half == 0 ? Wg : Wu;
+    CUtensorMap ta, tb;
+    const uint64_t dims[2] = {static_cast<uint64_t>(F), static_cast<uint64_t>(S)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(2 * F) * 2};
+    const uint32_t box[2] = {64, static_cast<uint32_t>(kPairBM / 2)};
+    if (!encode_tmap(&ta, dgu + half * F, 2, dims, strides, box)) return MGG_ERR_CUDA;
+    r.b_merged = H % 64 == 0 && tmap_weights_chunked(&tb, Wh, E, F, H);
+    if (!r.b_merged && !tmap_weights(&tb, Wh, E, F, H, 64, 64)) return MGG_ERR_CUDA;
+    if (timed(2 + half, st, [&] { return launch_rows_pair(kModeScatter, true, ta, tb, r, st); }) !=
+        cudaSuccess)
+      return MGG_ERR_CUDA;
+  }
+
+  // dWg_e = sum dg^T x, dWu_e = sum du^T x: the unpadded dg | du rows (rows
+  // past an expert's count meet zero-filled x rows and add nothing)
+  if (!dw_gemm(4, x, routing->row_token, H, dgu, S, F, 2 * F, routing->start, dWg) ||
+      !dw_gemm(5, x, routing->row_token, H, dgu + F, S, F, 2 * F, routing->start, dWu))
+    return MGG_ERR_CUDA;
+  return MGG_OK;
 }
 
 mgg_status mgg_debug_tile_schedule(const mgg_routing* routing, int E, int N, mgg_dtype dtype,

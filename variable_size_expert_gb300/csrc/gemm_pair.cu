@@ -63,7 +63,9 @@ constexpr int kEpiWarpsHi = 10;        // first warp of a second epilogue group 
 constexpr int DW_THREADS = 352;        // dynamic dW: the 320 above + warp 10, its tile scheduler
 // The dX GEMM (whose epilogue also gathers x for the d(routing weight) dot)
 // runs eight epilogue warps; the other row modes four.
-constexpr int rows_epi_warps(int mode) { return mode == kModeFusedDtopk ? 8 : 4; }
+constexpr int rows_epi_warps(int mode) {
+  return mode == kModeFusedDtopk || mode == kModeSwiGluBwd ? 8 : 4;
+}
 constexpr int rows_threads(int mode) { return rows_epi_warps(mode) == 8 ? 448 : NUM_THREADS; }
 constexpr int TMEM_COLS = 2 * PBN;
 constexpr int kRowsEpi = 16 * 1024;    // epilogue staging: 4 warps x 32 x 32 f32 or 8 x 32 x 16
@@ -183,6 +185,10 @@ __device__ __forceinline__ void pair_teardown(uint32_t tmem_base, int warp) {
 __device__ __forceinline__ float silu_fast(float v) {
   return __fdividef(v, 1.f + __expf(fminf(-v, 80.f)));
 }
+// sigmoid(v) = 1 / (1 + exp(-v)), the same way (the gated FFN backward)
+__device__ __forceinline__ float sigmoid_fast(float v) {
+  return __fdividef(1.f, 1.f + __expf(fminf(-v, 80.f)));
+}
 
 // ====================================================================== rows
 // F8: e4m3 operands (fused and bare modes, both K-major).  A stage still
@@ -195,9 +201,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
                      const __grid_constant__ CUtensorMap tmap_b, const RowsParams p) {
   // A rows gathered through row_token (else loaded in sorted order by TMA);
   // output added into token rows (else stored in sorted row order)
-  constexpr bool GATHER = MODE == kModeFused || MODE == kModeFusedDtopk || MODE == kModeGateUp;
+  constexpr bool GATEUP = MODE == kModeGateUp || MODE == kModeGateUpSave;
+  constexpr bool SAVE_GU = MODE == kModeGateUpSave;  // also store g and u (f32)
+  constexpr bool SWIGLU = MODE == kModeSwiGluBwd;    // gated FFN backward epilogue
+  constexpr bool DOT = MODE == kModeFusedDtopk || SWIGLU;  // d(routing weight) dot
+  constexpr bool GATHER =
+      MODE == kModeFused || MODE == kModeFusedDtopk || GATEUP || SWIGLU;
   constexpr bool SCATTER = MODE == kModeFused || MODE == kModeFusedDtopk || MODE == kModeScatter;
-  constexpr bool GATEUP = MODE == kModeGateUp;
   static_assert(!F8 || ((MODE == kModeFused || MODE == kModeBare) && !B_MN),
                 "e4m3 operands: fused and bare modes, K-major");
   constexpr int EPW = rows_epi_warps(MODE);  // epilogue warps
@@ -232,7 +242,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
   // The column halves of the last round pay off only where A arrives by TMA:
   // a half still needs all 256 gathered rows, and in the gather modes the
   // halves measured slower than the idle round they replace.
-  constexpr bool SPLIT = !GATHER;
+  constexpr bool SPLIT = !GATHER && !B_MN;
   const WorkPlan plan = work_plan(pair, npairs, total, SPLIT);
   const int nwork = plan.count();
   // Every role walks (wi, tau) together; without the split the work item is
@@ -448,6 +458,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
           o_own = __ldg(p.row_token + t.row0 + r_own);
           w_own = __ldg(p.row_weight + t.row0 + r_own);
           if (F8) w_own *= __ldg(p.a_scale + o_own);  // routing weight x token scale
+        } else if (SWIGLU && r_own < t.rows) {
+          w_own = __ldg(p.row_weight + t.row0 + r_own);  // sorted row, its routing weight
         } else if (F8 && r_own < t.rows) {
           w_own = __ldg(p.a_scale + t.row0 + r_own);  // row scale
         }
@@ -473,7 +485,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
                              static_cast<long long>(orow[j]) * p.ldx + col))
                        : make_uint2(0u, 0u);
       };
-      if (MODE == kModeFusedDtopk && half < nch) fetch_x(half, xb);
+      if (DOT && half < nch) fetch_x(half, xb);
       const int acc = tcount & 1;
       const uint32_t use = tcount >> 1;
       if (!__all_sync(0xffffffffu, wait_bar(m.acc_full + 8 * acc, use & 1, wc))) break;
@@ -486,44 +498,113 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
         // staging buffer like the f32 blocks, so every store instruction
         // writes four rows x 128 contiguous bytes of h.
         const int f0 = t.nb * (PBN / 2);
+        if constexpr (SAVE_GU) {
+          // as below, and g and u (f32, for the backward) also leave through
+          // the staging buffer, 32 x 32 blocks, four rows x 128 bytes per
+          // store; h of both 32-feature halves waits in registers meanwhile
 #pragma unroll 1
-        for (int cp = 0; cp < 2; ++cp) {
-#pragma unroll 1
-          for (int hb = 0; hb < 2; ++hb) {
-            const int c0 = cp * 64 + hb * 32;
-            float g[32], u[32];
-            tmem_ld32(taddr + c0, g);
-            tmem_ld32(taddr + PBN / 2 + c0, u);
-            tmem_ld_wait();
-            if (cp == 1 && hb == 1) {  // accumulator fully read
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
+          for (int cp = 0; cp < 2; ++cp) {
+            uint32_t hv[2][16];
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+              const int c0 = cp * 64 + hb * 32;
+              float g[32], u[32];
+              tmem_ld32(taddr + c0, g);
+              tmem_ld32(taddr + PBN / 2 + c0, u);
+              tmem_ld_wait();
+              if (cp == 1 && hb == 1) {  // accumulator fully read
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
+              }
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                hv[hb][i] = pack_bf16x2_rn(silu_fast(g[2 * i]) * u[2 * i],
+                                           silu_fast(g[2 * i + 1]) * u[2 * i + 1]);
+              const int f = f0 + c0 + 4 * kq;  // feature of this lane's four values
+              // a 32 x 32 block of v (lane = row) into columns off + f of gu
+              auto save = [&](const float(&v)[32], int off) {
+                __syncwarp();  // the previous block's reads are done
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                  st_shared_v4(stg + piece(lane, q), v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                               v[4 * q + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < LPR; ++j) {
+                  const int rl = rq + RSTEP * j;
+                  const float4 a = ld_shared_v4(stg + piece(rl, kq));
+                  if (ro + rl < t.rows && f < p.Nout)
+                    *reinterpret_cast<float4*>(p.guout +
+                                               static_cast<long long>(t.row0 + ro + rl) * p.ldgu +
+                                               off + f) = a;
+                }
+              };
+              save(g, 0);
+              save(u, p.Nout);
             }
-            uint32_t hv[16];
+            __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              hv[i] = pack_bf16x2_rn(silu_fast(g[2 * i]) * u[2 * i],
-                                     silu_fast(g[2 * i + 1]) * u[2 * i + 1]);
+            for (int hb = 0; hb < 2; ++hb)
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              st_shared_v4(stg + piece(lane, hb * 4 + q), __uint_as_float(hv[4 * q]),
-                           __uint_as_float(hv[4 * q + 1]), __uint_as_float(hv[4 * q + 2]),
-                           __uint_as_float(hv[4 * q + 3]));
+              for (int q = 0; q < 4; ++q)
+                st_shared_v4(stg + piece(lane, hb * 4 + q), __uint_as_float(hv[hb][4 * q]),
+                             __uint_as_float(hv[hb][4 * q + 1]), __uint_as_float(hv[hb][4 * q + 2]),
+                             __uint_as_float(hv[hb][4 * q + 3]));
+            __syncwarp();
+            const int col = f0 + cp * 64 + 8 * kq;
+#pragma unroll
+            for (int j = 0; j < LPR; ++j) {
+              const int rl = rq + RSTEP * j;
+              const float4 v = ld_shared_v4(stg + piece(rl, kq));
+              if (ro + rl < t.rows && col < p.Nout)
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.hout) +
+                                          static_cast<long long>(t.row0 + ro + rl) * p.ldh + col) =
+                    make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                               __float_as_uint(v.w));
+            }
+            __syncwarp();
           }
-          __syncwarp();
-          const int col = f0 + cp * 64 + 8 * kq;
+        } else {
+#pragma unroll 1
+          for (int cp = 0; cp < 2; ++cp) {
+#pragma unroll 1
+            for (int hb = 0; hb < 2; ++hb) {
+              const int c0 = cp * 64 + hb * 32;
+              float g[32], u[32];
+              tmem_ld32(taddr + c0, g);
+              tmem_ld32(taddr + PBN / 2 + c0, u);
+              tmem_ld_wait();
+              if (cp == 1 && hb == 1) {  // accumulator fully read
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
+              }
+              uint32_t hv[16];
 #pragma unroll
-          for (int j = 0; j < LPR; ++j) {
-            const int rl = rq + RSTEP * j;
-            const float4 v = ld_shared_v4(stg + piece(rl, kq));
-            if (ro + rl < t.rows && col < p.Nout)
-              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.hout) +
-                                        static_cast<long long>(t.row0 + ro + rl) * p.ldh + col) =
-                  make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
-                             __float_as_uint(v.w));
+              for (int i = 0; i < 16; ++i)
+                hv[i] = pack_bf16x2_rn(silu_fast(g[2 * i]) * u[2 * i],
+                                       silu_fast(g[2 * i + 1]) * u[2 * i + 1]);
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                st_shared_v4(stg + piece(lane, hb * 4 + q), __uint_as_float(hv[4 * q]),
+                             __uint_as_float(hv[4 * q + 1]), __uint_as_float(hv[4 * q + 2]),
+                             __uint_as_float(hv[4 * q + 3]));
+            }
+            __syncwarp();
+            const int col = f0 + cp * 64 + 8 * kq;
+#pragma unroll
+            for (int j = 0; j < LPR; ++j) {
+              const int rl = rq + RSTEP * j;
+              const float4 v = ld_shared_v4(stg + piece(rl, kq));
+              if (ro + rl < t.rows && col < p.Nout)
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.hout) +
+                                          static_cast<long long>(t.row0 + ro + rl) * p.ldh + col) =
+                    make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                               __float_as_uint(v.w));
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
         ++tcount;
         continue;
@@ -536,7 +617,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
       for (int cc = half; cc < nch; cc += EPW / 4) {
         const int col = n0 + cc * CW + 4 * kq;
         uint2 xn[LPR];
-        if (MODE == kModeFusedDtopk && cc + EPW / 4 < nch) fetch_x(cc + EPW / 4, xn);
+        if (DOT && cc + EPW / 4 < nch) fetch_x(cc + EPW / 4, xn);
+        // gated backward: this block's saved gate and up values, requested
+        // before the accumulator read so their latency overlaps it
+        float4 gq[SWIGLU ? LPR : 1], uq[SWIGLU ? LPR : 1];
+        if constexpr (SWIGLU) {
+#pragma unroll
+          for (int j = 0; j < LPR; ++j) {
+            const bool in = ro + rq + RSTEP * j < t.rows && col < p.Nout;
+            const float* gr = p.gu + static_cast<long long>(in ? orow[j] : 0) * p.ldgu + col;
+            gq[j] = in ? __ldg(reinterpret_cast<const float4*>(gr)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            uq[j] = in ? __ldg(reinterpret_cast<const float4*>(gr + p.Nout))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
         // e4m3: the expert's scales of this lane's four output columns
         float4 cs = make_float4(1.f, 1.f, 1.f, 1.f);
         if (F8 && col < p.Nout)
@@ -568,7 +662,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
             u.z *= cs.z;
             u.w *= cs.w;
           }
-          if (ro + rl < t.rows && col < p.Nout) {
+          if (SWIGLU && ro + rl < t.rows && col < p.Nout) {
+            // u = dy_b Wd_e for 4 features of the row: the d(routing weight)
+            // dot with the forward's bf16 h, then dh = w u and the SiLU-gated
+            // backward dg = dh u_up sigmoid(g) (1 + g (1 - sigmoid(g))),
+            // du = dh silu(g) from the saved f32 gate and up values, stored
+            // as bf16 (the operands of the dx and dW GEMMs)
+            dot[j] = fmaf(__uint_as_float(xb[j].x << 16), u.x, dot[j]);
+            dot[j] = fmaf(__uint_as_float(xb[j].x & 0xFFFF0000u), u.y, dot[j]);
+            dot[j] = fmaf(__uint_as_float(xb[j].y << 16), u.z, dot[j]);
+            dot[j] = fmaf(__uint_as_float(xb[j].y & 0xFFFF0000u), u.w, dot[j]);
+            const float gv[4] = {gq[j].x, gq[j].y, gq[j].z, gq[j].w};
+            const float uv[4] = {uq[j].x, uq[j].y, uq[j].z, uq[j].w};
+            const float av[4] = {u.x, u.y, u.z, u.w};
+            float dg[4], du[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float sg = sigmoid_fast(gv[q]);
+              const float dh = wgt[j] * av[q];
+              dg[q] = dh * uv[q] * (sg * (1.f + gv[q] * (1.f - sg)));
+              du[q] = dh * (gv[q] * sg);
+            }
+            __nv_bfloat16* hr = static_cast<__nv_bfloat16*>(p.hout) +
+                                static_cast<long long>(orow[j]) * p.ldh + col;
+            *reinterpret_cast<uint2*>(hr) =
+                make_uint2(pack_bf16x2_rn(dg[0], dg[1]), pack_bf16x2_rn(dg[2], dg[3]));
+            *reinterpret_cast<uint2*>(hr + p.Nout) =
+                make_uint2(pack_bf16x2_rn(du[0], du[1]), pack_bf16x2_rn(du[2], du[3]));
+          } else if (!SWIGLU && ro + rl < t.rows && col < p.Nout) {
             float* o = p.out + static_cast<long long>(orow[j]) * p.ldo + col;
             if (!SCATTER) {
               *reinterpret_cast<float4*>(o) =
@@ -586,7 +707,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
           }
         }
         __syncwarp();  // the block is read before the next one overwrites it
-        if (MODE == kModeFusedDtopk && cc + EPW / 4 < nch) {
+        if (DOT && cc + EPW / 4 < nch) {
 #pragma unroll
           for (int j = 0; j < LPR; ++j) xb[j] = xn[j];
         }
@@ -596,7 +717,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc_empty_l + 8 * acc);
       }
-      if (MODE == kModeFusedDtopk) {
+      if (DOT) {
         // the LPR lanes of a row hold partial sums over their columns (with
         // eight epilogue warps, both warps of a quadrant add theirs)
 #pragma unroll
@@ -1130,11 +1251,17 @@ cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_
     if (mode == kModeBare) return launch_rows_pair_t<kModeBare, false>(tmap_a, tmap_b, p, st);
     if (mode == kModeFused) return launch_rows_pair_t<kModeFused, false>(tmap_a, tmap_b, p, st);
     if (mode == kModeGateUp) return launch_rows_pair_t<kModeGateUp, false>(tmap_a, tmap_b, p, st);
+    if (mode == kModeGateUpSave)
+      return launch_rows_pair_t<kModeGateUpSave, false>(tmap_a, tmap_b, p, st);
     if (mode == kModeScatter)
       return launch_rows_pair_t<kModeScatter, false>(tmap_a, tmap_b, p, st);
   } else {
     if (mode == kModeFusedDtopk)
       return launch_rows_pair_t<kModeFusedDtopk, true>(tmap_a, tmap_b, p, st);
+    if (mode == kModeSwiGluBwd)
+      return launch_rows_pair_t<kModeSwiGluBwd, true>(tmap_a, tmap_b, p, st);
+    if (mode == kModeScatter)  // A rows by TMA, B read transposed (the gated FFN's dx)
+      return launch_rows_pair_t<kModeScatter, true>(tmap_a, tmap_b, p, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -57,7 +57,9 @@ enum RowsMode {
   kModeFused = 1,
   kModeFusedDtopk = 2,
   kModeGateUp = 3,
-  kModeScatter = 4
+  kModeScatter = 4,
+  kModeGateUpSave = 5,  // gate/up forward that also stores g and u (f32) for the backward
+  kModeSwiGluBwd = 6    // gated FFN backward: dh = w (dy Wd), then dg, du from the saved g, u
 };
 
 // One launch of the row-gathering grouped GEMM (forward, bare, dX).
@@ -86,6 +88,12 @@ struct RowsParams {
   // b_scale[e * Nout + n] (per expert and output column)
   const float* a_scale;
   const float* b_scale;
+  // gated FFN: gate/up saved by the forward, [rows, ldgu] f32, g in columns
+  // 0..Nout-1 and u in Nout..2 Nout-1 (written by kModeGateUpSave into guout,
+  // read by kModeSwiGluBwd from gu, which writes dg | du the same way into hout)
+  float* guout;
+  const float* gu;
+  int ldgu;
   int max_pairs;               // cap on the persistent grid's CTA pairs (0: all that fit)
   int32_t* dev_status;
   long long wait_limit;
@@ -163,6 +171,7 @@ cudaError_t launch_bwd_prep(const float* dy, int T, int N, int K, int k, const i
                             const float* row_weight, int E, int S_pad_max, void* dy_b, void* dyw,
                             float* dx, float* dtopk, cudaStream_t st,
                             int32_t* expert_order = nullptr, const DwSplitPlan* split = nullptr);
+cudaError_t launch_iota_ones(int32_t* iota, float* ones, int n, cudaStream_t st);
 cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* start, int E, int BM,
                                   int max_tiles, int32_t* out, cudaStream_t st);
 

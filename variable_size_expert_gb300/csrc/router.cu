@@ -760,6 +760,23 @@ cudaError_t launch_bwd_prep(const float* dy, int T, int N, int K, int k, const i
                     reinterpret_cast<float4*>(dx), dtopk, order, sp);
 }
 
+// iota[i] = i and ones[i] = 1 for i < n: the identity row map and unit row
+// weights through which the gated FFN backward reuses the dW GEMM (over the
+// sorted h rows) and the scatter GEMM (dx, whose rows carry no weight).
+__global__ void iota_ones_kernel(int32_t* __restrict__ iota, float* __restrict__ ones, int n) {
+  pdl_trigger();
+  pdl_wait();  // the previous call's kernels may still read these arrays
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    iota[i] = i;
+    ones[i] = 1.f;
+  }
+}
+
+cudaError_t launch_iota_ones(int32_t* iota, float* ones, int n, cudaStream_t st) {
+  const int blocks = std::max(1, std::min(cdiv(n, 256), num_sms() * 4));
+  return launch_pdl(iota_ones_kernel, dim3(blocks), dim3(256), 0, st, iota, ones, n);
+}
+
 cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* start, int E, int BM,
                                   int max_tiles, int32_t* out, cudaStream_t st) {
   if (max_tiles <= 0) return cudaSuccess;

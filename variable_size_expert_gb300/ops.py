@@ -171,9 +171,11 @@ def moe_ffn_forward(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: tor
                     expert_ids: torch.Tensor, topk_weights: torch.Tensor,
                     status: torch.Tensor | None = None, out: torch.Tensor | None = None,
                     h: torch.Tensor | None = None, routing: RoutingBuffers | None = None,
-                    workspace: torch.Tensor | None = None):
+                    workspace: torch.Tensor | None = None, gu: torch.Tensor | bool | None = None):
     """Gated expert FFN forward (bf16).  Returns (y [T, H] float32, h [T*k, F]
-    bf16 in expert-sorted row order, routing)."""
+    bf16 in expert-sorted row order, routing), and with ``gu`` (True, or a
+    float32 [T*k, 2F] buffer) also gu, the gate and up projections the
+    backward needs: (y, h, routing, gu)."""
     lib = L.load()
     if x.dtype != torch.bfloat16 or not (Wg.dtype == Wu.dtype == Wd.dtype == torch.bfloat16):
         raise TypeError("the gated FFN path takes bfloat16 x and weights")
@@ -192,11 +194,46 @@ def moe_ffn_forward(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: tor
     nbytes = lib.mgg_workspace_bytes(L.MGG_OP_FFN_FORWARD, T, k, E, H, F, L.MGG_BF16)
     ws = workspace if workspace is not None and workspace.numel() >= nbytes else _workspace(nbytes, dev)
     rs = r.struct()
+    gub = None
+    if gu is not None and gu is not False:
+        gub = gu if isinstance(gu, torch.Tensor) else torch.empty(T * k, 2 * F, dtype=torch.float32,
+                                                                  device=dev)
     L.check(lib.mgg_moe_ffn_forward(_ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(ids), _ptr(w), T,
-                                    H, F, E, k, L.MGG_BF16, _ptr(y), _ptr(hb), ctypes.byref(rs),
+                                    H, F, E, k, L.MGG_BF16, _ptr(y), _ptr(hb),
+                                    _ptr(gub) if gub is not None else None, ctypes.byref(rs),
                                     _ptr(st), _ptr(ws), ws.numel(), _stream()),
             "mgg_moe_ffn_forward")
-    return y, hb, r
+    return (y, hb, r) if gub is None else (y, hb, r, gub)
+
+
+def moe_ffn_backward(dy: torch.Tensor, x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor,
+                     Wd: torch.Tensor, h: torch.Tensor, gu: torch.Tensor, routing: RoutingBuffers,
+                     k: int, status: torch.Tensor | None = None, dx=None, dWg=None, dWu=None,
+                     dWd=None, dtopk=None, workspace: torch.Tensor | None = None):
+    """Gated expert FFN backward (bf16) from the training forward's h and gu.
+    Returns (dx [T, H], dWg [E, F, H], dWu [E, F, H], dWd [E, H, F],
+    dtopk [T, k]), all float32."""
+    lib = L.load()
+    T, H = x.shape
+    E, F, _ = Wg.shape
+    dev = x.device
+    dy = dy.contiguous().float()
+    f32 = dict(dtype=torch.float32, device=dev)
+    dx = dx if dx is not None else torch.empty(T, H, **f32)
+    dWg = dWg if dWg is not None else torch.empty(E, F, H, **f32)
+    dWu = dWu if dWu is not None else torch.empty(E, F, H, **f32)
+    dWd = dWd if dWd is not None else torch.empty(E, H, F, **f32)
+    dtopk = dtopk if dtopk is not None else torch.empty(T, k, **f32)
+    st = status if status is not None else new_status(dev)
+    nbytes = lib.mgg_workspace_bytes(L.MGG_OP_FFN_BACKWARD, T, k, E, H, F, L.MGG_BF16)
+    ws = workspace if workspace is not None and workspace.numel() >= nbytes else _workspace(nbytes, dev)
+    rs = routing.struct()
+    L.check(lib.mgg_moe_ffn_backward(_ptr(dy), _ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(h),
+                                     _ptr(gu), ctypes.byref(rs), T, H, F, E, k, L.MGG_BF16,
+                                     _ptr(dx), _ptr(dWg), _ptr(dWu), _ptr(dWd), _ptr(dtopk),
+                                     _ptr(st), _ptr(ws), ws.numel(), _stream()),
+            "mgg_moe_ffn_backward")
+    return dx, dWg, dWu, dWd, dtopk
 
 
 def moe_backward(dy: torch.Tensor, x: torch.Tensor, W: torch.Tensor, routing: RoutingBuffers,

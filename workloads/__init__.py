@@ -165,14 +165,15 @@ def moe_problem(T: int, K: int, N: int, E: int, k: int, seed: int = 0,
 
 def ffn_problem(T: int, H: int, F: int, E: int, k: int, seed: int = 0,
                 routing: str = "uniform", zipf_s: float = 1.2,
-                weights: str = "uniform") -> dict:
+                weights: str = "uniform", with_dy: bool = False) -> dict:
     """One gated expert-FFN problem ("Grouped GEMM for MoE, in depth",
     §Choosing an implementation: gate and up projections, then the down
     projection).
 
     x[T,H] bf16 ~N(0,1); Wg, Wu [E,F,H] bf16 ~N(0,1/H); Wd [E,H,F] bf16
     ~N(0,1/F); expert_ids[T,k] int32 and topk_weights[T,k] fp32 drawn as in
-    ``moe_problem`` (same ``routing`` and ``weights`` choices).
+    ``moe_problem`` (same ``routing`` and ``weights`` choices); optionally
+    dy[T,H] fp32 ~N(0,1), drawn last.
     """
     rng = np.random.default_rng(seed)
     x = _normal(rng, (T, H))
@@ -193,11 +194,14 @@ def ffn_problem(T: int, H: int, F: int, E: int, k: int, seed: int = 0,
         w = _softmax_weights(rng, T, k)
     else:
         raise ValueError(weights)
-    return {
+    out = {
         "x": to_bf16(x), "Wg": to_bf16(Wg), "Wu": to_bf16(Wu), "Wd": to_bf16(Wd),
         "expert_ids": torch.from_numpy(ids_), "topk_weights": torch.from_numpy(w),
         "T": T, "H": H, "F": F, "E": E, "k": k,
     }
+    if with_dy:
+        out["dy"] = torch.from_numpy(_normal(rng, (T, H)))
+    return out
 
 
 def decode_problem(E: int = 128, M_max: int = 64, K: int = 7168, N: int = 2048,
@@ -244,3 +248,4 @@ BWD_HOT = dict(T=8192, K=1024, N=1024, E=8, k=2, seed=0, routing="hot", weights=
                with_dy=True)
 # gated expert FFN, top-2: hidden 2048, FFN width 2048 (gate + up = 4096 columns)
 FFN_TOP2 = dict(T=4096, H=2048, F=2048, E=8, k=2, seed=0, routing="uniform", weights="uniform")
+FFN_BWD_TOP2 = dict(FFN_TOP2, with_dy=True)
