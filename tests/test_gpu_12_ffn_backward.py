@@ -113,3 +113,14 @@ def test_ffn_backward_reuses_workspace_and_repeats():
         assert mgg.read_status(st) == 0
         for name, g_, r_ in zip(NAMES, got, _oracle(p)):
             assert_bf16_close(g_, r_, name)
+
+
+def test_ffn_backward_side_by_side_option(monkeypatch):
+    """MGG_FFN_BWD_SPLIT runs dh beside dWd and dx beside dWg, dWu on
+    disjoint CTA-pair sets (off by default, measured slower): same results."""
+    monkeypatch.setenv("MGG_FFN_BWD_SPLIT", "0.55,0.4")
+    p = workloads.ffn_problem(T=300, H=256, F=256, E=8, k=2, seed=8, routing="uniform",
+                              with_dy=True)
+    *_, got = _fwd_bwd(_dev(p), fill=float("nan"))
+    for name, g_, r_ in zip(NAMES, got, _oracle(p)):
+        assert_bf16_close(g_, r_, name)

@@ -1,6 +1,7 @@
 // C ABI of the library (declared in include/mgg.h): argument checks,
 // workspace carving, tensor-map encoding and stream-ordered launch
 // sequences.  Nothing here allocates, frees or synchronises.
+#include <stdio.h>
 #include <stdlib.h>
 
 #include <algorithm>
@@ -96,6 +97,23 @@ int bwd_dx_pairs(int P, long long S, int E, int K, int N) {
     }
   }
   return best;
+}
+
+// CTA pairs of the gated FFN backward's main-stream GEMMs in its two
+// side-by-side phases (the rest go to the side stream): dh with the SwiGLU
+// backward beside dWd, then dx beside dWg and dWu.  Off by default: on the
+// top-2 FFN workload the seven GEMMs one after the other on all pairs took
+// 491 us, side by side 712-735 us over the shares tried.
+// MGG_FFN_BWD_SPLIT="a,b" (shares in (0, 1) of the pairs for dh and for dx)
+// turns it on.
+void ffn_bwd_pairs(int P, int* a1, int* a2) {
+  *a1 = *a2 = 0;
+  const char* e = getenv("MGG_FFN_BWD_SPLIT");
+  if (!e || P < 2) return;
+  double x = 0.0, y = 0.0;
+  if (sscanf(e, "%lf,%lf", &x, &y) != 2 || !(x > 0.0 && x < 1.0 && y > 0.0 && y < 1.0)) return;
+  *a1 = std::min(P - 1, std::max(1, static_cast<int>(P * x + 0.5)));
+  *a2 = std::min(P - 1, std::max(1, static_cast<int>(P * y + 0.5)));
 }
 
 // One side stream and a fork/join event pair per host thread and device,
@@ -967,15 +985,13 @@ mgg_status mgg_moe_ffn_backward(const float* dy, const void* x, const void* Wg, 
   CUtensorMap tm_wd;
   p.b_merged = F % 64 == 0 && tmap_weights_chunked(&tm_wd, Wd, E, H, F);
   if (!p.b_merged && !tmap_weights(&tm_wd, Wd, E, H, F, 64, 64)) return MGG_ERR_CUDA;
-  if (timed(0, st, [&] { return launch_rows_pair(kModeSwiGluBwd, true, tm_wd, tm_wd, p, st); }) !=
-      cudaSuccess)
-    return MGG_ERR_CUDA;
 
   // dW GEMMs over a [rows, N] bf16 operand b (row stride ld) for the
   // experts' rows starting at bstart: dWd over h (identity row map) and the
   // scaled dy; dWg, dWu over x (gathered by token) and the dg, du halves
   auto dw_gemm = [&](int slot, const void* a, const int32_t* a_rows, int Ka, const void* b,
-                     int rows, int N, int ld, const int32_t* bstart, float* out) -> bool {
+                     int rows, int N, int ld, const int32_t* bstart, float* out, int pairs,
+                     cudaStream_t ss) -> bool {
     DwParams q{};
     q.x = a;
     q.K = Ka;
@@ -988,6 +1004,7 @@ mgg_status mgg_moe_ffn_backward(const float* dy, const void* x, const void* Wg, 
     q.E = E;
     q.dW = out;
     q.expert_order = order;
+    q.max_pairs = pairs;
     q.dev_status = dev_status;
     q.wait_limit = wait_limit();
     CUtensorMap tb, to;
@@ -1005,14 +1022,11 @@ mgg_status mgg_moe_ffn_backward(const float* dy, const void* x, const void* Wg, 
       if (!encode_tmap(&tb, b, 2, dims, strides, box)) return false;
     }
     if (!tmap_dw_store(&to, out, E, N, Ka)) return false;
-    return timed(slot, st, [&] { return launch_dw_pair(tb, to, q, st); }) == cudaSuccess;
+    return timed(slot, ss, [&] { return launch_dw_pair(tb, to, q, ss); }) == cudaSuccess;
   };
-  // dWd_e = sum (w dy)^T h: the padded scaled dy rows (prep) against h
-  if (!dw_gemm(1, h, iota, F, dyw, L.b.S_pad_max, H, H, pstart, dWd)) return MGG_ERR_CUDA;
-
   // dx[t] += dg Wg_e and du Wu_e: dg | du rows by TMA (sorted order), the
   // weights read transposed, unit row weights, added into the token rows
-  for (int half = 0; half < 2; ++half) {
+  auto dx_gemm = [&](int half, int pairs, cudaStream_t ss) -> bool {
     RowsParams r{};
     r.Kc = F;
     r.lda = 2 * F;
@@ -1024,6 +1038,7 @@ mgg_status mgg_moe_ffn_backward(const float* dy, const void* x, const void* Wg, 
     r.Nout = H;
     r.out = dx;
     r.ldo = H;
+    r.max_pairs = pairs;
     r.dev_status = dev_status;
     r.wait_limit = wait_limit();
     const void* Wh = half == 0 ? Wg : Wu;
@@ -1031,18 +1046,48 @@ mgg_status mgg_moe_ffn_backward(const float* dy, const void* x, const void* Wg, 
     const uint64_t dims[2] = {static_cast<uint64_t>(F), static_cast<uint64_t>(S)};
     const uint64_t strides[1] = {static_cast<uint64_t>(2 * F) * 2};
     const uint32_t box[2] = {64, static_cast<uint32_t>(kPairBM / 2)};
-    if (!encode_tmap(&ta, dgu + half * F, 2, dims, strides, box)) return MGG_ERR_CUDA;
+    if (!encode_tmap(&ta, dgu + half * F, 2, dims, strides, box)) return false;
     r.b_merged = H % 64 == 0 && tmap_weights_chunked(&tb, Wh, E, F, H);
-    if (!r.b_merged && !tmap_weights(&tb, Wh, E, F, H, 64, 64)) return MGG_ERR_CUDA;
-    if (timed(2 + half, st, [&] { return launch_rows_pair(kModeScatter, true, ta, tb, r, st); }) !=
-        cudaSuccess)
-      return MGG_ERR_CUDA;
-  }
-
+    if (!r.b_merged && !tmap_weights(&tb, Wh, E, F, H, 64, 64)) return false;
+    return timed(2 + half, ss,
+                 [&] { return launch_rows_pair(kModeScatter, true, ta, tb, r, ss); }) == cudaSuccess;
+  };
+  auto dh_gemm = [&](int pairs, cudaStream_t ss) -> bool {
+    p.max_pairs = pairs;
+    return timed(0, ss, [&] {
+             return launch_rows_pair(kModeSwiGluBwd, true, tm_wd, tm_wd, p, ss);
+           }) == cudaSuccess;
+  };
+  // dWd_e = sum (w dy)^T h: the padded scaled dy rows (prep) against h
+  auto dwd = [&](int pairs, cudaStream_t ss) {
+    return dw_gemm(1, h, iota, F, dyw, L.b.S_pad_max, H, H, pstart, dWd, pairs, ss);
+  };
   // dWg_e = sum dg^T x, dWu_e = sum du^T x: the unpadded dg | du rows (rows
   // past an expert's count meet zero-filled x rows and add nothing)
-  if (!dw_gemm(4, x, routing->row_token, H, dgu, S, F, 2 * F, routing->start, dWg) ||
-      !dw_gemm(5, x, routing->row_token, H, dgu + F, S, F, 2 * F, routing->start, dWu))
+  auto dwgu = [&](int pairs, cudaStream_t ss) {
+    return dw_gemm(4, x, routing->row_token, H, dgu, S, F, 2 * F, routing->start, dWg, pairs,
+                   ss) &&
+           dw_gemm(5, x, routing->row_token, H, dgu + F, S, F, 2 * F, routing->start, dWu, pairs,
+                   ss);
+  };
+  const int P = num_sms() / 2;
+  int a1 = 0, a2 = 0;
+  ffn_bwd_pairs(P, &a1, &a2);
+  if (a1 <= 0) {
+    if (!dh_gemm(0, st) || !dwd(0, st) || !dx_gemm(0, 0, st) || !dx_gemm(1, 0, st) || !dwgu(0, st))
+      return MGG_ERR_CUDA;
+    return MGG_OK;
+  }
+  // side by side on disjoint sets of CTA pairs: dh (main) beside dWd
+  // (side), then, once dh is done, dx (main) beside dWg and dWu (side)
+  SideStream* f = side_stream();
+  if (!f) return MGG_ERR_CUDA;
+  if (cudaEventRecord(f->fork, st) != cudaSuccess ||
+      cudaStreamWaitEvent(f->side, f->fork, 0) != cudaSuccess || !dwd(P - a1, f->side) ||
+      !dh_gemm(a1, st) || cudaEventRecord(f->fork, st) != cudaSuccess ||
+      cudaStreamWaitEvent(f->side, f->fork, 0) != cudaSuccess || !dwgu(P - a2, f->side) ||
+      !dx_gemm(0, a2, st) || !dx_gemm(1, a2, st) || cudaEventRecord(f->join, f->side) != cudaSuccess ||
+      cudaStreamWaitEvent(st, f->join, 0) != cudaSuccess)
     return MGG_ERR_CUDA;
   return MGG_OK;
 }
