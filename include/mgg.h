@@ -392,7 +392,8 @@ mgg_status mgg_moe_ffn_forward(const void* x, const void* Wg, const void* Wu, co
  *   dx[t]     += dg Wg_e + du Wu_e                              [H]
  *   dWg_e     += dg^T x[t],  dWu_e += du^T x[t]                 [F, H]
  *   dWd_e     += bf16(fl32(w[t,j] dy[t]))^T h[r]                [H, F]
- * (the forward's rounding of h to bf16 is taken as the identity).  Seven
+ * (the forward's rounding of h to bf16 is taken as the identity; the dh
+ * epilogue recomputes the forward's bf16 h bit for bit from g and u).  Seven
  * grouped GEMM launches after one pass over dy: dh with the SwiGLU backward
  * in its epilogue (dy rows gathered by token, Wd read transposed), dWd (the
  * dW GEMM over the sorted h rows), dx in two scatter GEMMs (dg | du rows,

@@ -110,3 +110,66 @@ def test_fp8_forward_graph_replay_matches_eager():
         torch.cuda.synchronize()
         assert torch.equal(got, ref)
         assert np.isfinite(got.cpu().numpy()).all()
+
+
+def test_ffn_training_step_graph_replay_matches_eager():
+    """The gated FFN training step (forward keeping g and u, then the
+    backward's seven GEMMs) captures too; replays on new inputs give the
+    eager calls' bits for y, h, gu and the weight gradients dWd, dWg, dWu
+    (no atomics), and dx and d(routing weight) to float32 rounding."""
+    def prob(seed):
+        p = workloads.ffn_problem(T=300, H=256, F=192, E=6, k=2, seed=seed, routing="random",
+                                  with_dy=True)
+        return {n: p[n].to(DEV) for n in ("x", "Wg", "Wu", "Wd", "expert_ids", "topk_weights", "dy")}
+    a, b = prob(10), prob(11)
+    T, H = a["x"].shape
+    E, F, _ = a["Wg"].shape
+    k = a["expert_ids"].shape[1]
+    buf = {n: t.clone() for n, t in a.items()}
+    y = torch.empty(T, H, device=DEV)
+    h = torch.empty(T * k, F, dtype=torch.bfloat16, device=DEV)
+    gu = torch.empty(T * k, 2 * F, device=DEV)
+    r = mgg.RoutingBuffers.empty(T, k, E, DEV)
+    outs = dict(dx=torch.empty(T, H, device=DEV), dWg=torch.empty(E, F, H, device=DEV),
+                dWu=torch.empty(E, F, H, device=DEV), dWd=torch.empty(E, H, F, device=DEV),
+                dtopk=torch.empty(T, k, device=DEV))
+    st = mgg.new_status(DEV)
+    ws_f = torch.empty(mgg.workspace_bytes(L.MGG_OP_FFN_FORWARD, T, k, E, H, F), dtype=torch.uint8,
+                       device=DEV)
+    ws_b = torch.empty(mgg.workspace_bytes(L.MGG_OP_FFN_BACKWARD, T, k, E, H, F),
+                       dtype=torch.uint8, device=DEV)
+
+    def step():
+        mgg.moe_ffn_forward(buf["x"], buf["Wg"], buf["Wu"], buf["Wd"], buf["expert_ids"],
+                            buf["topk_weights"], status=st, out=y, h=h, routing=r, workspace=ws_f,
+                            gu=gu)
+        mgg.moe_ffn_backward(buf["dy"], buf["x"], buf["Wg"], buf["Wu"], buf["Wd"], h, gu, r, k,
+                             status=st, workspace=ws_b, **outs)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for src in (a, b):
+        for n in buf:
+            buf[n].copy_(src[n])
+        g.replay()
+        torch.cuda.synchronize()
+        got = {"y": y.clone(), "h": h.clone(), "gu": gu.clone(), **{n: t.clone() for n, t in outs.items()}}
+        y2, h2, r2, gu2 = mgg.moe_ffn_forward(src["x"], src["Wg"], src["Wu"], src["Wd"],
+                                              src["expert_ids"], src["topk_weights"], gu=True)
+        ref = dict(zip(("dx", "dWg", "dWu", "dWd", "dtopk"),
+                       mgg.moe_ffn_backward(src["dy"], src["x"], src["Wg"], src["Wu"], src["Wd"],
+                                            h2, gu2, r2, k)))
+        torch.cuda.synchronize()
+        for n, t in (("y", y2), ("h", h2), ("gu", gu2), ("dWd", ref["dWd"]), ("dWg", ref["dWg"]),
+                     ("dWu", ref["dWu"])):
+            assert torch.equal(got[n], t), n
+        for n in ("dx", "dtopk"):
+            torch.testing.assert_close(got[n], ref[n], rtol=1e-5,
+                                       atol=1e-5 * float(ref[n].abs().max()))
+    assert mgg.read_status(st) == 0

@@ -959,9 +959,10 @@ mgg_status mgg_moe_ffn_backward(const float* dy, const void* x, const void* Wg, 
                       L.b.S_pad_max, dy_b, dyw, dx, dtopk, st, order) != cudaSuccess)
     return MGG_ERR_CUDA;
 
-  // dh = w (bf16(dy) Wd_e), with the d(routing weight) dot against the
-  // forward's h, then dg | du from the saved g, u: the dX GEMM's main loop
-  // (dy rows gathered by token, Wd read transposed) with the gated epilogue
+  // dh = w (bf16(dy) Wd_e), with the d(routing weight) dot against h (the
+  // epilogue recomputes the forward's bf16 h from the saved g, u), then
+  // dg | du: the dX GEMM's main loop (dy rows gathered by token, Wd read
+  // transposed) with the gated epilogue
   RowsParams p{};
   p.A = dy_b;
   p.lda = H;
@@ -973,8 +974,6 @@ mgg_status mgg_moe_ffn_backward(const float* dy, const void* x, const void* Wg, 
   p.start = routing->start;
   p.E = E;
   p.Nout = F;
-  p.xdot = h;
-  p.ldx = F;
   p.dtopk = dtopk;
   p.gu = gu;
   p.ldgu = 2 * F;

@@ -205,6 +205,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
   constexpr bool SAVE_GU = MODE == kModeGateUpSave;  // also store g and u (f32)
   constexpr bool SWIGLU = MODE == kModeSwiGluBwd;    // gated FFN backward epilogue
   constexpr bool DOT = MODE == kModeFusedDtopk || SWIGLU;  // d(routing weight) dot
+  // the dot's other operand read from memory (dX: x); the gated backward
+  // recomputes h from the saved g and u instead
+  constexpr bool FETCH_X = MODE == kModeFusedDtopk;
   constexpr bool GATHER =
       MODE == kModeFused || MODE == kModeFusedDtopk || GATEUP || SWIGLU;
   constexpr bool SCATTER = MODE == kModeFused || MODE == kModeFusedDtopk || MODE == kModeScatter;
@@ -485,7 +488,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
                              static_cast<long long>(orow[j]) * p.ldx + col))
                        : make_uint2(0u, 0u);
       };
-      if (DOT && half < nch) fetch_x(half, xb);
+      if (FETCH_X && half < nch) fetch_x(half, xb);
       const int acc = tcount & 1;
       const uint32_t use = tcount >> 1;
       if (!__all_sync(0xffffffffu, wait_bar(m.acc_full + 8 * acc, use & 1, wc))) break;
@@ -617,7 +620,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
       for (int cc = half; cc < nch; cc += EPW / 4) {
         const int col = n0 + cc * CW + 4 * kq;
         uint2 xn[LPR];
-        if (DOT && cc + EPW / 4 < nch) fetch_x(cc + EPW / 4, xn);
+        if (FETCH_X && cc + EPW / 4 < nch) fetch_x(cc + EPW / 4, xn);
         // gated backward: this block's saved gate and up values, requested
         // before the accumulator read so their latency overlaps it
         float4 gq[SWIGLU ? LPR : 1], uq[SWIGLU ? LPR : 1];
@@ -664,20 +667,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
           }
           if (SWIGLU && ro + rl < t.rows && col < p.Nout) {
             // u = dy_b Wd_e for 4 features of the row: the d(routing weight)
-            // dot with the forward's bf16 h, then dh = w u and the SiLU-gated
-            // backward dg = dh u_up sigmoid(g) (1 + g (1 - sigmoid(g))),
-            // du = dh silu(g) from the saved f32 gate and up values, stored
-            // as bf16 (the operands of the dx and dW GEMMs)
-            dot[j] = fmaf(__uint_as_float(xb[j].x << 16), u.x, dot[j]);
-            dot[j] = fmaf(__uint_as_float(xb[j].x & 0xFFFF0000u), u.y, dot[j]);
-            dot[j] = fmaf(__uint_as_float(xb[j].y << 16), u.z, dot[j]);
-            dot[j] = fmaf(__uint_as_float(xb[j].y & 0xFFFF0000u), u.w, dot[j]);
+            // dot with h, recomputed from the saved f32 gate and up values
+            // exactly as the forward rounded it (the same bits), then
+            // dh = w u and the SiLU-gated backward dg = dh u_up sigmoid(g)
+            // (1 + g (1 - sigmoid(g))), du = dh silu(g), stored as bf16 (the
+            // operands of the dx and dW GEMMs)
             const float gv[4] = {gq[j].x, gq[j].y, gq[j].z, gq[j].w};
             const float uv[4] = {uq[j].x, uq[j].y, uq[j].z, uq[j].w};
             const float av[4] = {u.x, u.y, u.z, u.w};
             float dg[4], du[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
+              const uint32_t hb = pack_bf16x2_rn(silu_fast(gv[q]) * uv[q], 0.f);
+              dot[j] = fmaf(__uint_as_float(hb << 16), av[q], dot[j]);
               const float sg = sigmoid_fast(gv[q]);
               const float dh = wgt[j] * av[q];
               dg[q] = dh * uv[q] * (sg * (1.f + gv[q] * (1.f - sg)));
@@ -707,7 +709,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
           }
         }
         __syncwarp();  // the block is read before the next one overwrites it
-        if (DOT && cc + EPW / 4 < nch) {
+        if (FETCH_X && cc + EPW / 4 < nch) {
 #pragma unroll
           for (int j = 0; j < LPR; ++j) xb[j] = xn[j];
         }
