@@ -28,7 +28,7 @@ __all__ = [
     "schedule_stats", "grouped_gemm", "moe_forward", "moe_forward_unfused",
     "moe_backward", "moe_backward_rows", "moe_backward_dw_rows", "masked_grouped_gemm",
     "moe_loss", "rel_frobenius", "max_abs_ratio", "silu", "moe_ffn_forward", "moe_ffn_backward",
-    "moe_ffn_loss",
+    "moe_ffn_loss", "moe_ffn_backward_rows", "moe_ffn_backward_dw_rows",
     "E4M3_MAX", "e4m3_decode", "e4m3_encode", "quantize_fp8_rows", "grouped_gemm_fp8",
     "moe_forward_fp8", "masked_grouped_gemm_fp8",
 ]
@@ -445,6 +445,65 @@ def moe_ffn_backward(x, Wg, Wu, Wd, expert_ids, topk_weights, dy, bf16_operands=
             dWu[e] += du.T @ xt
             dWd[e] += _dyw_operand(w32[t, j], dy32[t], bf16_operands).T @ h
     return dx, dWg, dWu, dWd, dtopk
+
+
+def moe_ffn_backward_rows(x, Wg, Wu, Wd, expert_ids, topk_weights, dy, tokens,
+                          bf16_operands=True):
+    """dx[tokens] and dtopk[tokens] by the definitions of ``moe_ffn_backward``
+    (sampled checks at full size)."""
+    ids = np.asarray(expert_ids)
+    w32 = np.asarray(topk_weights, dtype=np.float32)
+    x = np.asarray(x, dtype=np.float64)
+    dy32 = np.asarray(dy, dtype=np.float32)
+    rnd = bf16_round if bf16_operands else (lambda a: np.asarray(a, dtype=np.float64))
+    tok = np.asarray(tokens)
+    dx = np.zeros((tok.size, x.shape[1]))
+    dtopk = np.zeros((tok.size, ids.shape[1]))
+    for i, t in enumerate(tok):
+        dyb = rnd(dy32[t])
+        for j in range(ids.shape[1]):
+            e = ids[t, j]
+            Wge = np.asarray(Wg[e], dtype=np.float64)
+            Wue = np.asarray(Wu[e], dtype=np.float64)
+            g, u = Wge @ x[t], Wue @ x[t]
+            s = 1.0 / (1.0 + np.exp(-g))
+            a_dy = dyb @ np.asarray(Wd[e], dtype=np.float64)
+            dtopk[i, j] = a_dy @ rnd(g * s * u)
+            dh = np.float64(w32[t, j]) * a_dy
+            dx[i] += rnd(dh * u * s * (1.0 + g * (1.0 - s))) @ Wge + rnd(dh * g * s) @ Wue
+    return dx, dtopk
+
+
+def moe_ffn_backward_dw_rows(x, Wg, Wu, Wd, expert_ids, topk_weights, dy, which, pairs,
+                             bf16_operands=True):
+    """Rows of one weight gradient of ``moe_ffn_backward``: which = "g", "u"
+    (dWg[e, f, :], dWu[e, f, :] for (e, f) in pairs) or "d" (dWd[e, n, :] for
+    (e, n) in pairs), each a sum over expert e's assignments."""
+    ids = np.asarray(expert_ids)
+    w32 = np.asarray(topk_weights, dtype=np.float32)
+    x = np.asarray(x, dtype=np.float64)
+    dy32 = np.asarray(dy, dtype=np.float32)
+    rnd = bf16_round if bf16_operands else (lambda a: np.asarray(a, dtype=np.float64))
+    out = np.zeros((len(pairs), Wd.shape[2] if which == "d" else x.shape[1]))
+    for i, (e, c) in enumerate(pairs):
+        t, j = np.nonzero(ids == e)
+        if t.size == 0:
+            continue
+        xt = x[t]
+        Wde = np.asarray(Wd[e], dtype=np.float64)
+        if which == "d":
+            g = xt @ np.asarray(Wg[e], dtype=np.float64).T
+            u = xt @ np.asarray(Wu[e], dtype=np.float64).T
+            h = rnd(g / (1.0 + np.exp(-g)) * u)
+            out[i] = _dyw_operand(w32[t, j], dy32[t, c][:, None], bf16_operands)[:, 0] @ h
+            continue
+        g = xt @ np.asarray(Wg[e][c], dtype=np.float64)
+        u = xt @ np.asarray(Wu[e][c], dtype=np.float64)
+        s = 1.0 / (1.0 + np.exp(-g))
+        dh = w32[t, j].astype(np.float64) * (rnd(dy32[t]) @ Wde[:, c])
+        d = rnd(dh * u * s * (1.0 + g * (1.0 - s))) if which == "g" else rnd(dh * g * s)
+        out[i] = d @ xt
+    return out
 
 
 def moe_ffn_loss(dy, x, Wg, Wu, Wd, expert_ids, topk_weights) -> float:

@@ -102,3 +102,33 @@ class _XView:
     def __getitem__(self, idx):
         e, rows = idx
         return self.x[e, rows].float().numpy().astype(np.float64)
+
+
+def test_ffn_train_step_top2_full_sampled():
+    """Gated FFN training step at the size bench.py times (T=4096, H=F=2048,
+    E=8, top-2): y in full against the forward oracle, then the backward's
+    dx and dtopk on 24 sampled tokens and dWg, dWu, dWd on 3 sampled rows of
+    every expert, against the oracle's restrictions (pinned to its full
+    definition)."""
+    p = workloads.ffn_problem(**workloads.FFN_BWD_TOP2)
+    d = {n: p[n].to(DEV) for n in ("x", "Wg", "Wu", "Wd", "expert_ids", "topk_weights", "dy")}
+    st = mgg.new_status(DEV)
+    y, h, r, gu = mgg.moe_ffn_forward(d["x"], d["Wg"], d["Wu"], d["Wd"], d["expert_ids"],
+                                      d["topk_weights"], status=st, gu=True)
+    dx, dWg, dWu, dWd, dtopk = mgg.moe_ffn_backward(d["dy"], d["x"], d["Wg"], d["Wu"], d["Wd"], h,
+                                                    gu, r, 2, status=st)
+    torch.cuda.synchronize()
+    assert mgg.read_status(st) == 0
+    args = (f64(p["x"]), f64(p["Wg"]), f64(p["Wu"]), f64(p["Wd"]), p["expert_ids"].numpy(),
+            p["topk_weights"].numpy(), p["dy"].numpy())
+    rng = np.random.default_rng(0)
+    tok = np.sort(rng.choice(p["T"], 24, replace=False))
+    rdx, rdt = O.moe_ffn_backward_rows(*args, tok)
+    assert_bf16_close(dx[tok], rdx, "dx (sampled tokens)")
+    assert_bf16_close(dtopk[tok], rdt, "dtopk (sampled tokens)")
+    E, F, H = p["E"], p["F"], p["H"]
+    for which, got, width in (("g", dWg, F), ("u", dWu, F), ("d", dWd, H)):
+        pairs = [(e, int(c)) for e in range(E) for c in rng.choice(width, 3, replace=False)]
+        ref = O.moe_ffn_backward_dw_rows(*args, which, pairs)
+        sel = torch.stack([got[e, c] for e, c in pairs])
+        assert_bf16_close(sel, ref, f"dW{which} (sampled rows)")

@@ -170,3 +170,18 @@ def test_ffn_backward_planted_mistakes_are_caught():
                 variant(lambda g: sig(g) * (1 - sig(g))),       # sigmoid's own derivative
                 variant(lambda g: sig(g) * (1 + g * (1 - sig(g))), swap_gu=True)):
         assert O.rel_frobenius(bad, ref[1]) > 1e-3
+
+
+def test_ffn_backward_restrictions_match_full():
+    """The sampled-row forms equal the full oracle on the same inputs."""
+    x, Wg, Wu, Wd, ids, w, dy = _problem(11, 8, 16, 4, 2, seed=12)
+    full = O.moe_ffn_backward(x, Wg, Wu, Wd, ids, w, dy)
+    tok = [7, 0, 10, 3]
+    dx, dtopk = O.moe_ffn_backward_rows(x, Wg, Wu, Wd, ids, w, dy, tok)
+    np.testing.assert_allclose(dx, full[0][tok], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dtopk, full[4][tok], rtol=1e-12, atol=1e-13)
+    for which, ref in (("g", full[1]), ("u", full[2]), ("d", full[3])):
+        pairs = [(e, c) for e in range(4) for c in (0, ref.shape[1] - 1, 3)]
+        got = O.moe_ffn_backward_dw_rows(x, Wg, Wu, Wd, ids, w, dy, which, pairs)
+        np.testing.assert_allclose(got, np.stack([ref[e, c] for e, c in pairs]), rtol=1e-12,
+                                   atol=1e-13)
