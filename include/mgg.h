@@ -39,6 +39,23 @@
  *   alignment) and 16-byte aligned base pointers.  The f32 path takes any
  *   K, N >= 1 and 4-byte aligned pointers.
  * - Only sm_103 devices are accepted (MGG_ERR_UNSUPPORTED_ARCH otherwise).
+ *
+ * Environment switches (read when a call is made; none changes a result
+ * beyond f32 rounding):
+ *   MGG_WAIT_LIMIT     SM clock cycles a pipeline wait may take before the
+ *                      kernel gives up and sets MGG_DEV_TIMEOUT (read once;
+ *                      default about a second)
+ *   MGG_ROUTER=block   route with one block instead of the cooperative
+ *                      multi-block router
+ *   MGG_BWD_SPLIT      mgg_moe_backward's share of CTA pairs for dX beside dW
+ *                      (0: one after the other)
+ *   MGG_DW_SPLITK      most pieces of one expert's dW contraction (0 or 1: no
+ *                      split)
+ *   MGG_DW_SCHEDULE=dynamic  dW tiles from an atomic work queue instead of
+ *                      the static longest-first order
+ *   MGG_FFN_BWD_SPLIT="a,b"  mgg_moe_ffn_backward's GEMMs side by side on
+ *                      shares a (dh) and b (dx) of the CTA pairs (default:
+ *                      one after the other)
  */
 #ifndef MGG_H
 #define MGG_H
