@@ -446,6 +446,15 @@ mgg_status mgg_debug_tile_schedule(const mgg_routing* routing, int E, int N, mgg
                                    int max_tiles, int32_t* out, void* stream);
 
 /*
+ * Test of the bounded wait every pipeline uses (failure detection without a
+ * GPU fault): one thread waits, with the kernels' own wait helper and a limit
+ * of limit_cycles SM clock cycles (1 .. 2^40), on an mbarrier that nothing
+ * arrives on.  The wait runs out, MGG_DEV_TIMEOUT is OR-ed into *dev_status
+ * and the kernel returns, leaving the context usable.  Stream-ordered.
+ */
+mgg_status mgg_debug_wait_timeout(int32_t* dev_status, long long limit_cycles, void* stream);
+
+/*
  * Benchmark instrumentation (no counterpart on the pages).  With n > 0,
  * later calls record events[2*i] right before and events[2*i+1] right after
  * the launch of their i-th main GEMM kernel, on the call's stream:

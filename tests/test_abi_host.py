@@ -160,6 +160,14 @@ def test_ffn_backward_invalid_arguments_rejected_before_launch(lib):
                                    fake, 1 << 30, None) == L.MGG_ERR_ALIGNMENT
 
 
+def test_wait_timeout_entry_checks_arguments(lib):
+    from variable_size_expert_gb300 import _lib as L
+    fake = ctypes.c_void_p(0x10000)
+    assert lib.mgg_debug_wait_timeout(None, 1000, None) == L.MGG_ERR_INVALID_ARG
+    assert lib.mgg_debug_wait_timeout(fake, 0, None) == L.MGG_ERR_INVALID_ARG
+    assert lib.mgg_debug_wait_timeout(fake, 1 << 41, None) == L.MGG_ERR_INVALID_ARG
+
+
 def test_product_path_has_no_oracle_or_fallback():
     """The package never imports the oracle, and fails loudly without its library."""
     pkg = os.path.join(ROOT, "variable_size_expert_gb300")

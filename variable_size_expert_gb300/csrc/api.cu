@@ -1105,6 +1105,13 @@ mgg_status mgg_debug_tile_schedule(const mgg_routing* routing, int E, int N, mgg
                                          static_cast<cudaStream_t>(stream)));
 }
 
+mgg_status mgg_debug_wait_timeout(int32_t* dev_status, long long limit_cycles, void* stream) {
+  if (!dev_status || limit_cycles < 1 || limit_cycles > (1LL << 40)) return MGG_ERR_INVALID_ARG;
+  mgg_status s = check_arch();
+  if (s != MGG_OK) return s;
+  return from_cuda(launch_wait_timeout(dev_status, limit_cycles, static_cast<cudaStream_t>(stream)));
+}
+
 mgg_status mgg_set_kernel_events(void* const* events, int n) {
   if (n < 0 || n > 8) return MGG_ERR_INVALID_ARG;
   if (!events || n == 0) {

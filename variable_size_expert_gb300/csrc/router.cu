@@ -777,6 +777,27 @@ cudaError_t launch_iota_ones(int32_t* iota, float* ones, int n, cudaStream_t st)
   return launch_pdl(iota_ones_kernel, dim3(blocks), dim3(256), 0, st, iota, ones, n);
 }
 
+// The pipelines' bounded wait on its own: one thread waits, with the kernels'
+// wait helper and the given cycle limit, on a fresh mbarrier that nothing
+// arrives on.  The wait runs out, records kDevTimeout in *dev_status and the
+// kernel returns (no copies or MMAs are in flight).
+__global__ void wait_timeout_kernel(int32_t* dev_status, long long limit) {
+  __shared__ alignas(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  const WaitCtl wc{&abort_flag, dev_status, limit};
+  (void)wait_bar(b, 0, wc);  // phase 0 never completes: one arrival expected, none made
+}
+
+cudaError_t launch_wait_timeout(int32_t* dev_status, long long limit, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(dev_status, limit);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* start, int E, int BM,
                                   int max_tiles, int32_t* out, cudaStream_t st) {
   if (max_tiles <= 0) return cudaSuccess;
