@@ -240,8 +240,7 @@ def run_ours(args, ws, rank, local):
     # timed region: exactly K steps, each a replay of the captured step
     barrier(ws)
     torch.cuda.synchronize()
-    clk = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv")
-                       if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None).start()
+    clk = ClockSampler(local, args.clocks_csv).start()
     wall0 = time.perf_counter()
     for _ in range(args.steps):
         if args.flush_mb:
@@ -984,6 +983,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="also keep the raw nvidia-smi clock samples of the timed region here")
     ap.add_argument("--cpu-reps", type=int, default=4)
     ap.add_argument("--flush-mb", type=int, default=512, help="L2 flush buffer between timed steps")
     args = ap.parse_args()
