@@ -1105,6 +1105,15 @@ mgg_status mgg_debug_tile_schedule(const mgg_routing* routing, int E, int N, mgg
                                          static_cast<cudaStream_t>(stream)));
 }
 
+}  // extern "C"
+
+namespace mgg {
+// router.cu: the bounded-wait test kernel
+cudaError_t launch_wait_timeout(int32_t* dev_status, long long limit, cudaStream_t st);
+}  // namespace mgg
+
+extern "C" {
+
 mgg_status mgg_debug_wait_timeout(int32_t* dev_status, long long limit_cycles, void* stream) {
   if (!dev_status || limit_cycles < 1 || limit_cycles > (1LL << 40)) return MGG_ERR_INVALID_ARG;
   mgg_status s = check_arch();

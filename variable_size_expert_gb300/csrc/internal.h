@@ -172,7 +172,6 @@ cudaError_t launch_bwd_prep(const float* dy, int T, int N, int K, int k, const i
                             float* dx, float* dtopk, cudaStream_t st,
                             int32_t* expert_order = nullptr, const DwSplitPlan* split = nullptr);
 cudaError_t launch_iota_ones(int32_t* iota, float* ones, int n, cudaStream_t st);
-cudaError_t launch_wait_timeout(int32_t* dev_status, long long limit, cudaStream_t st);
 cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* start, int E, int BM,
                                   int max_tiles, int32_t* out, cudaStream_t st);
 
