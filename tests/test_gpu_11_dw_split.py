@@ -187,3 +187,20 @@ def test_split_side_by_side_default(monkeypatch):
     (dx, dW, dtopk), _ = _backward(p, dW_fill=float("nan"))
     for nm, got, rf in zip(("dx", "dW", "dtopk"), (dx, dW, dtopk), _ref(p)):
         assert_bf16_close(got, rf, nm)
+
+
+def test_split_with_dynamic_queue(monkeypatch):
+    """The dynamic dW work queue (MGG_DW_SCHEDULE=dynamic) hands out the
+    split pieces too: the live tiles are the prefix up to the experts with
+    rows; results meet the oracle like the static schedule's."""
+    monkeypatch.setenv("MGG_BWD_SPLIT", "0")
+    monkeypatch.setenv("MGG_DW_SCHEDULE", "dynamic")
+    p = _problem("hot_ragged")                         # a split expert and an empty one
+    (dx, dW, dtopk), r = _backward(p, dW_fill=float("nan"))
+    for nm, got, rf in zip(("dx", "dW", "dtopk"), (dx, dW, dtopk), _ref(p)):
+        assert_bf16_close(got, rf, nm)
+    counts = r.counts.cpu().tolist()
+    dWc = dW.cpu()
+    for e in range(len(counts)):
+        if counts[e] == 0:
+            assert torch.all(dWc[e] == 0) and not torch.any(torch.signbit(dWc[e]))
