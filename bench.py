@@ -12,9 +12,12 @@ the fused backward (dX with d routing weight, dW).  Useful FLOPs per step =
 Prints ONE JSON line (rank 0).  Timing: W untimed warm-up steps, then K
 timed steps; a 512 MiB buffer is written between timed steps to flush the
 129 MB L2; each step and each main GEMM is timed with CUDA events on the
-launching stream; the reported time is the max over ranks.  Extras on the
-same line: the skewed forward, the masked decode (CUDA-graph replay, GB/s)
-and the small bare grouped GEMM.
+launching stream; the reported time is the max over ranks.  On the same
+line, "extras" holds the other measurements (gated FFN, e4m3, dW split,
+dynamic dW queue) and the last key, "configs", one compact entry per
+workload: 1 bare E=4 (latency), 2 forward top-2, 3 skewed forward, 4
+backward top-2, 5 masked decode (CUDA-graph replay, GB/s), each with its
+fraction of the measured peak.
 """
 from __future__ import annotations
 
@@ -181,9 +184,11 @@ def run_ours(args, ws, rank, local):
     ev_f, ev_b = Events(1), Events(2)
     hf, hb = ev_f.handles(), ev_b.handles()
 
-    def step():
+    def step(mid=None):
         lib.mgg_set_kernel_events(hf, 1)
         mgg.moe_forward(x, W, ids, w, status=status, out=y, routing=routing, workspace=ws_f)
+        if mid is not None:
+            mid.record()
         lib.mgg_set_kernel_events(hb, 2)
         mgg.moe_backward(dy, x, W, routing, k, status=status, dx=dx, dW=dW, dtopk=dtopk, workspace=ws_b)
         lib.mgg_set_kernel_events(None, 0)
@@ -195,7 +200,8 @@ def run_ours(args, ws, rank, local):
         raise RuntimeError(f"device status {mgg.read_status(status)} after warm-up")
 
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_step, t_fwd, t_dx, t_dw, t_graph = [], [], [], [], []
+    sm = torch.cuda.Event(enable_timing=True)
+    t_step, t_fwd, t_dx, t_dw, t_graph, t_fcall = [], [], [], [], [], []
 
     # the same step captured once as a CUDA graph (the library reads no size
     # back to the host, so route + forward + backward capture as one graph)
@@ -225,10 +231,11 @@ def run_ours(args, ws, rank, local):
         if args.flush_mb:
             flush.zero_()
         s0.record()
-        step()
+        step(sm)
         s1.record()
         torch.cuda.synchronize()
         t_step.append(s0.elapsed_time(s1))
+        t_fcall.append(s0.elapsed_time(sm))
         t_fwd.append(ev_f.ms(0))
         t_dx.append(ev_b.ms(0))
         t_dw.append(ev_b.ms(1))
@@ -303,6 +310,7 @@ def run_ours(args, ws, rank, local):
                      "peak": peak_tf, "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
                      "peak_source": f"{peak_kind} bf16 dense (burst)",
                      "traffic": traffic,
+                     "traffic_note": TRAFFIC_NOTES.get(dom),
                      "algorithmic_gflop_per_launch": round(gemm_flops / 1e9, 3)},
         "kernels_ms": {kname: round(v, 4) for kname, v in kern.items()},
         "kernels_tflops": {kname: round(gemm_flops / (v * 1e-3) / 1e12, 1) for kname, v in kern.items()},
@@ -312,15 +320,38 @@ def run_ours(args, ws, rank, local):
     }
     if rank == 0 and not args.no_e2e:
         out["e2e"] = run_e2e(args, p, dev, lib, mgg, L, flops_step)
-    if rank == 0 and not args.no_extras:
-        out["extras"] = run_extras(dev, mgg, L, lib, peaks, peak_kind, flush)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_reps)
+    # one compact entry per workload (bare E=4, forward top-2, skewed
+    # forward, backward top-2, masked decode), printed last so that it stays
+    # in view at the end of the line
+    configs = {"2_fwd_top2": {
+        "ms": round(statistics.mean(t_fcall), 4),
+        "tflops": round(gemm_flops / (statistics.mean(t_fcall) * 1e-3) / 1e12, 1),
+        "gemm_ms": round(kern["fwd_gather_scatter_gemm"], 4),
+        "gemm_frac": round(gemm_flops / (kern["fwd_gather_scatter_gemm"] * 1e-3) / 1e12 / peak_tf, 4)}}
+    if rank == 0 and not args.no_extras:
+        out["extras"], more = run_extras(dev, mgg, L, lib, peaks, peak_kind, flush, peak_tf)
+        configs.update(more)
+        configs["4_bwd_top2"].update(
+            {f"{n}_gemm_frac": round(gemm_flops / (kern[kn] * 1e-3) / 1e12 / peak_tf, 4)
+             for n, kn in (("dx", "bwd_dx_dtopk_gemm"), ("dw", "bwd_dw_gemm"))})
+    out["configs"] = dict(sorted(configs.items()))
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+# What the DRAM traffic figures of the GEMMs leave out (ncu counts the bytes
+# that reached DRAM during the launch, not those still in L2)
+TRAFFIC_NOTES = {
+    "bwd_dw_gemm": ("undercounts writes: part of dW's f32 output (134 MB) is still dirty in the "
+                    "write-back L2 when the kernel ends"),
+    "fwd_gather_scatter_gemm": ("includes reading back y (33.6 MB): the router zeroes y and the "
+                                "epilogue's atomic adds fetch those lines again"),
+}
 
 
 def load_traffic(kernel: str):
@@ -439,7 +470,10 @@ def run_e2e(args, p, dev, lib, mgg, L, flops_step):
                      "three streams (copy in / compute / copy out)")}
 
 
-def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
+def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush, peak_tf):
+    """The other workloads.  Returns (extras, configs): the detailed figures,
+    and one compact entry for each of the bare E=4, skewed forward, top-2
+    backward and masked decode workloads."""
     # per-kernel rates on the whole GPU: dX and dW one after the other
     prev_split = os.environ.get("MGG_BWD_SPLIT")
     os.environ["MGG_BWD_SPLIT"] = "0"
@@ -453,7 +487,20 @@ def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
     res["bwd_split"] = _bwd_split_extra(dev, mgg, flush)
     res["dw_splitk"] = _dw_splitk_extra(dev, mgg, lib, flush)
     res["ffn_backward"] = _ffn_backward_extra(dev, mgg, lib, flush)
-    return res
+    fs, dec, be, bs = res["fwd_skew"], res["decode"], res["bare_e4"], res["bwd_split"]
+    bwd_fl = 4.0 * 4096 * 2 * 2048 * 2048
+    configs = {
+        "1_bare_e4": {"us": be["us_per_call"],
+                      "tflops": round(2.0 * 256 * 128 * 96 / (be["us_per_call"] * 1e-6) / 1e12, 3)},
+        "3_fwd_skew": {"ms": fs["ms"], "tflops": fs["tflops"], "gemm_ms": fs["gemm_ms"],
+                       "gemm_frac": round(fs["gemm_tflops"] / peak_tf, 4),
+                       "useful_rows": fs["useful_row_fraction"]},
+        "4_bwd_top2": {"ms": bs["side_by_side_ms"],
+                       "tflops": round(bwd_fl / (bs["side_by_side_ms"] * 1e-3) / 1e12, 1),
+                       "frac": round(bwd_fl / (bs["side_by_side_ms"] * 1e-3) / 1e12 / peak_tf, 4)},
+        "5_decode": {"ms": dec["ms"], "GB/s": dec["GB/s"], "frac": dec["roofline"]["frac"]},
+    }
+    return res, configs
 
 
 def _ffn_backward_extra(dev, mgg, lib, flush):
@@ -513,7 +560,6 @@ def _ffn_backward_extra(dev, mgg, lib, flush):
         "backward_tflops": round(6 * fl_unit / (t_bwd * 1e-3) / 1e12, 1),
         "backward_useful_gflop": round(6 * fl_unit / 1e9, 2),
         "gemm_tflops": {n: round(fl_unit / (m * 1e-3) / 1e12, 1) for n, m in zip(names, med)},
-        "gemm_us": {n: round(m * 1e3, 1) for n, m in zip(names, med)},
     }
 
 
@@ -562,7 +608,7 @@ def _dw_splitk_extra(dev, mgg, lib, flush):
         counts = r.counts.cpu().tolist()
         k = ids.shape[1]
         fl = 2.0 * c["T"] * k * c["K"] * c["N"]
-        row = {"counts": counts}
+        row = {"max_count": max(counts)}
         for tag, split in (("split", None), ("unsplit", "0")):
             with _Env(MGG_DW_SPLITK=split, MGG_BWD_SPLIT="0"):
                 for _ in range(3):
@@ -844,7 +890,10 @@ def _run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(gbs / hbm, 4), "peak_source": f"{peak_kind} copy bandwidth",
                      "traffic": load_traffic("masked_decode_gemm")},
-        "timing": "CUDA-graph replay, 20 replays"}
+        "timing": "CUDA-graph replay, 20 replays",
+        "inputs": ("masked_m drawn by numpy (seed 0) as in the parity tests; x and W drawn with "
+                   "torch's seeded CUDA generator (same shapes and distributions) to keep start-up "
+                   "short")}
     # the same decode on e4m3 codes (weights quantised per (expert, channel),
     # activations per row): half the weight bytes to stream
     xv = torch.nan_to_num(x, nan=0.0)
@@ -958,13 +1007,15 @@ def run_reference(args, ws, rank):
     times = d["times"][args.warmup:]
     t = statistics.mean(times)
     value = d["flops"] / t / 1e12
-    sample = (f"float64 numpy oracle, forward + backward of {tokens} tokens of the workload "
-              f"(same K, N, E, k) per step")
+    sample = (f"float64 numpy oracle, forward + backward of the first {tokens} of the workload's "
+              f"4096 tokens (same K, N, E, k) per step: a subsample, so the arm's TFLOP/s is that "
+              f"of a smaller problem")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "TFLOP/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "sample_tokens": tokens},
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample_tokens": tokens,
+                                        "same_config": False},
         "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,

@@ -206,7 +206,10 @@ mgg_status mgg_route(const int32_t* expert_ids, const float* topk_weights, int T
  *     larger problems return MGG_ERR_WORKSPACE without launching.
  *   - The first call on a device looks up that device's array address
  *     (cudaGetSymbolAddress, with the device current); make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the life of the
+ *     process: do not use this entry point on a device after a
+ *     cudaDeviceReset (or any other teardown of its primary context), since
+ *     the kept address then belongs to the old context.
  *   - All calls on a device share the one array and it keeps the last
  *     call's contents; the router overwrites every entry it reads, so no
  *     clearing is needed.  Calls whose work overlaps on the GPU (other

@@ -914,8 +914,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
       return hist[i & 3];
     };
     // Stage cursor over (tile, k-block), skipping experts with no rows.  The
-    // row tokens of a stage are fetched two stages ahead of its copies, so
-    // the dependent loads stay off the issue path.
+    // row tokens of a stage are requested three stages ahead of its copies,
+    // so the dependent loads stay off the issue path.
     struct Cur {
       int i, tau, kb, nkb, m, s0, k0, kb0;
     };
@@ -958,24 +958,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
     load(pf, tk2);
     int it = 0;
     bool ok = true;
-    while (ok && cur.tau < total) {
+    // One stage: copies from the tokens in `tk`, then the tokens of the stage
+    // three ahead loaded into `tk`.  The three arrays rotate by call, so no
+    // register is copied from a load still in flight (a move of a pending
+    // load stalls the warp until it lands: one stage of latency instead of
+    // three).
+    auto stage = [&](int (&tk)[4]) -> bool {
+      if (!ok || cur.tau >= total) return false;
       const int s = it % STAGES;
       const uint32_t ph = (it / STAGES) & 1;
       if (!__all_sync(0xffffffffu, wait_bar(m.empty + 8 * s, ph ^ 1, wc))) {
         ok = false;
-        break;
+        return false;
       }
       const uint32_t dst = m.sA + s * A_STAGE;
+      if ((cur.kb0 + cur.kb + 1) * BK <= cur.m && cur.k0 + CBM <= p.K) {
+        // every row of the stage is one of the expert's and every column
+        // inside K: plain copies
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < CBM / 64; ++j) {
-          const int kcol = cur.k0 + 64 * j + c * 8;
-          const bool go = tk0[i] >= 0 && kcol < p.K;
-          cp_async_16(dst + j * CHUNK + sw128_offset(rr + 16 * i, c),
-                      go ? static_cast<const void*>(X + static_cast<long long>(tk0[i]) * p.K + kcol)
-                         : p.x,
-                      go ? 16u : 0u);
+          for (int j = 0; j < CBM / 64; ++j)
+            cp_async_16_full(dst + j * CHUNK + sw128_offset(rr + 16 * i, c),
+                             X + static_cast<long long>(tk[i]) * p.K + cur.k0 + 64 * j + c * 8);
+      } else {
+        // an expert's last stage or the K edge: rows past the expert's count
+        // are zero-filled (the padded dY rows they meet are zero, and stale
+        // values must not turn that into NaN)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+          for (int j = 0; j < CBM / 64; ++j) {
+            const int kcol = cur.k0 + 64 * j + c * 8;
+            const bool go = tk[i] >= 0 && kcol < p.K;
+            cp_async_16(dst + j * CHUNK + sw128_offset(rr + 16 * i, c),
+                        go ? static_cast<const void*>(X + static_cast<long long>(tk[i]) * p.K + kcol)
+                           : p.x,
+                        go ? 16u : 0u);
+          }
         }
       }
       cp_async_commit();
@@ -986,14 +1006,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
         if (lane == 0) mbar_arrive(m.gathered + 8 * ((it - LAG) % STAGES));
       }
       ++it;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        tk0[i] = tk1[i];
-        tk1[i] = tk2[i];
-      }
       step(cur);
       step(pf);
-      load(pf, tk2);
+      load(pf, tk);
+      return true;
+    };
+    while (stage(tk0) && stage(tk1) && stage(tk2)) {
     }
     cp_async_wait<0>();
     fence_proxy_async_smem();

@@ -57,7 +57,7 @@ extern "C" mgg_status mgg_route_noalloc(const int32_t* expert_ids, const float* 
     return MGG_ERR_INVALID_ARG;
   if (T < 1 || k < 1 || E < 1 || N < 1 || E > kMaxExperts) return MGG_ERR_INVALID_ARG;
   if (static_cast<long long>(T) * k > (1LL << 30)) return MGG_ERR_INVALID_ARG;
-  if (dtype != MGG_BF16 && dtype != MGG_F32) return MGG_ERR_DTYPE;
+  if (dtype != MGG_BF16 && dtype != MGG_F32 && dtype != MGG_FP8_E4M3) return MGG_ERR_DTYPE;
   // the fixed array must hold the per-chunk histogram
   if (route_ws_bytes(T, k, E) > kScratchBytes) return MGG_ERR_WORKSPACE;
   // only sm_103 images are built: check before touching the device symbol
