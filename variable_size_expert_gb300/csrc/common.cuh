@@ -124,6 +124,17 @@ __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, lo
   return true;
 }
 
+// The same with acquire at cluster scope (the phase publishes data the peer
+// CTA stored into this CTA's shared memory).
+__device__ __forceinline__ bool wait_bar_cluster_drain(uint32_t bar, uint32_t parity,
+                                                       long long limit) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (clock64() - t0 > limit) return false;
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------- PDL
 // Programmatic dependent launch.  A kernel launched with launch_pdl may be
 // scheduled while the previous kernel in the stream is still running (once
@@ -456,6 +467,15 @@ __device__ __forceinline__ void tma_load_4d_cg2(uint32_t dst, const CUtensorMap*
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
       "l"(map), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
+}
+// Remote arrival with an expected transaction count, relaxed at cluster
+// scope: a CTA announces the bytes its own copies will deliver to an
+// mbarrier in the other CTA of its pair.
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                   cluster_addr),
+               "r"(bytes)
+               : "memory");
 }
 // Copy `bytes` (multiple of 16) of this CTA's shared memory into another
 // CTA's shared memory (`dst` and `bar` are cluster addresses); completion is

@@ -27,15 +27,18 @@
 // the weight bytes each SM pulls per FLOP, and the kernels are bound by the
 // bytes L2 can deliver to the SMs.
 //
-// Barriers: full[s] lives in the leader and counts the leader's expect-tx
-// arrival, the TMA bytes of both CTAs and (gather modes) the peer's relay
-// arrival (see relay_stage); gathered[s] in each CTA counts that CTA's four
-// gather warps; empty[s] and acc_full[a] live in both CTAs and are
-// signalled by the leader's multicast commits; acc_empty[a] lives in the
-// leader and counts both CTAs' four epilogue warps.
+// Barriers: full[s] lives in the leader and counts one expect-tx arrival
+// from each CTA's TMA thread (each announcing its own bytes), the TMA bytes
+// of both CTAs and, in the gather modes, one arrival per gather warp of both
+// CTAs: the leader's MMA waits on that one barrier per stage (a second wait
+// per stage measured 8% slower on the fused forward).  empty[s] and
+// acc_full[a] live in both CTAs and are signalled by the leader's multicast
+// commits; acc_empty[a] lives in the leader and counts both CTAs' epilogue
+// warps; pdone (leader) collects every producer's count of issued stages at
+// teardown (see pair_drain).
 //
 // Roles per CTA (320 threads): warps 0-3 epilogue, warp 4 TMEM allocation
-// (both CTAs), MMA issue (leader) or the gather relay (peer), warp 5 TMA for
+// (both CTAs) and MMA issue (leader), warp 5 TMA for
 // B (and A in bare mode), warps 6-9 gather A rows with cp.async (gather
 // modes); the dX GEMM adds a second epilogue group, warps 10-13 (448
 // threads); the dW GEMM adds warp 10, its dynamic tile scheduler (352).
@@ -71,7 +74,7 @@ constexpr int TMEM_COLS = 2 * PBN;
 constexpr int kRowsEpi = 16 * 1024;    // epilogue staging: 4 warps x 32 x 32 f32 or 8 x 32 x 16
 constexpr int DW_EPI_BUF = 32 * 32 * 4;  // one warp's 32 (n) x 32 (k) f32 block
 constexpr int kDwEpi = 4 * 2 * DW_EPI_BUF;  // double-buffered per epilogue warp
-constexpr int kBarBytes = 512;
+constexpr int kBarBytes = 640;
 constexpr int TR = 16;  // dynamic tile ring slots (dW)
 template <int STAGES, int EPI_BYTES>
 constexpr size_t smem_bytes() {
@@ -84,7 +87,8 @@ constexpr long long DRAIN_LIMIT = 200000000LL;
 
 
 struct PairSmem {
-  uint32_t sA, sB, sEpi, full, empty, gathered, acc_full, acc_empty, drain;
+  uint32_t sA, sB, sEpi, full, empty, acc_full, acc_empty, drain, pdone;
+  uint32_t issued;               // producers' counts of issued stages (9 ints)
   uint32_t tfull, tempty, tids;  // dynamic tile ring: barriers and tile ids
   uint32_t* tmem_slot;
   volatile int* abort_flag;
@@ -92,8 +96,8 @@ struct PairSmem {
 
 template <int STAGES, int EPI_BYTES>
 __device__ __forceinline__ PairSmem carve(uint8_t* smem_raw) {
-  constexpr int NUM_BARS = 3 * STAGES + 5 + 2 * TR;
-  static_assert(NUM_BARS * 8 + 8 + 4 * TR <= kBarBytes, "barrier area");
+  constexpr int NUM_BARS = 2 * STAGES + 6 + 2 * TR;
+  static_assert(NUM_BARS * 8 + 48 + 4 * TR <= kBarBytes, "barrier area");
   PairSmem m;
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -104,52 +108,98 @@ __device__ __forceinline__ PairSmem carve(uint8_t* smem_raw) {
   const uint32_t bar0 = m.sEpi + EPI_BYTES;
   m.full = bar0;
   m.empty = bar0 + 8 * STAGES;
-  m.gathered = bar0 + 16 * STAGES;
-  m.acc_full = bar0 + 24 * STAGES;
+  m.acc_full = bar0 + 16 * STAGES;
   m.acc_empty = m.acc_full + 16;
   m.drain = m.acc_full + 32;
-  m.tfull = m.drain + 8;
+  m.pdone = m.drain + 8;
+  m.tfull = m.pdone + 8;
   m.tempty = m.tfull + 8 * TR;
   m.tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar0 - base) + 8 * NUM_BARS);
   m.abort_flag = reinterpret_cast<volatile int*>(m.tmem_slot + 1);
-  m.tids = bar0 + 8 * NUM_BARS + 8;
+  m.issued = bar0 + 8 * NUM_BARS + 8;
+  m.tids = bar0 + 8 * NUM_BARS + 48;
   return m;
 }
 
-// The peer CTA's gathered rows reach the leader through a relay: its gather
-// warps arrive on the peer's own gathered[s] (CTA scope) once their copies
-// have completed (cp.async.wait_group) and been fenced into the async proxy,
-// and one otherwise idle thread of the peer waits there and forwards a
-// single relaxed cluster-scope arrival to the leader's full[s].  The data is
-// already complete in the peer's shared memory when the relay observes the
-// local phase, so the forward carries no release fence: a release at cluster
-// scope costs a memory barrier per stage and measured 1.5x slower overall.
-// The leader's MMA thread waits on its own gathered[s] directly.
+// Every TMA copy of a stage, the peer's included, completes on the leader's
+// full[s]: the copies write the issuing CTA's own shared memory and count
+// their bytes on the leader's barrier, each CTA's TMA thread announcing its
+// own bytes with one expect-tx arrival (the leader's locally before its
+// copies, the peer's as a relaxed cluster-scope arrival after them).  A
+// relay of the peer's completion through a peer thread measured 7% slower
+// on the bare GEMM.
+//
+// No CTA may exit while a copy it issued can still land in its shared
+// memory.  The teardown cluster barrier keeps the peer alive until the
+// leader arrives there, and before that the leader's TMA thread waits, in
+// pair_drain, for every copy either CTA issued.  Every producer (both TMA
+// threads and, in the gather modes, the eight gather warps) reports how many
+// stages it issued (a store into the leader's shared memory, then a release
+// arrival on pdone; a gather warp has arrived for every stage it issued, its
+// own copies landed).  For each stage at most STAGES behind the furthest one
+// issued, the leader makes the arrivals of the producers that stopped before
+// it (they loaded nothing for it, so no bytes are owed) and waits for the
+// phase: it completes exactly when the copies that were issued have landed.
+// Older stages have completed already: their slots were refilled, which
+// needs the MMAs that waited on them.  On the normal path every producer
+// issued the same stages and nothing is added.  Every wait is bounded.
+constexpr int kIssuedSlots = 9;  // [0] the peer's TMA thread, [1 + 4 rank + w] gather warp w
+__device__ __forceinline__ void report_issued(const PairSmem& m, int slot, int issued) {
+  st_cluster_s32(mapa_shared(m.issued + 4 * slot, 0), issued);
+  mbar_arrive_cluster(mapa_shared(m.pdone, 0));
+}
 template <int STAGES>
-__device__ __forceinline__ bool relay_stage(const PairSmem& m, uint32_t full_l, int it,
-                                            const WaitCtl& wc) {
-  const int s = it % STAGES;
-  if (!wait_bar(m.gathered + 8 * s, (it / STAGES) & 1, wc)) return false;
-  mbar_arrive_cluster_relaxed(full_l + 8 * s);
-  return true;
+__device__ __forceinline__ void pair_drain(const PairSmem& m, bool leader, bool gather,
+                                           int issued) {
+  if (!leader) {
+    report_issued(m, 0, issued);
+    return;
+  }
+  int cnt[kIssuedSlots + 1];
+  const int nrep = gather ? kIssuedSlots : 1;
+  cnt[0] = issued;
+  const bool reported = wait_bar_cluster_drain(m.pdone, 0, DRAIN_LIMIT);
+  int hi = issued;
+  for (int r = 0; r < nrep; ++r) {
+    cnt[1 + r] = reported ? ld_shared_s32(m.issued + 4 * r) : issued;
+    hi = std::max(hi, cnt[1 + r]);
+  }
+  for (int j = std::max(0, hi - STAGES); j < hi; ++j) {
+    const uint32_t b = m.full + 8 * (j % STAGES);
+    for (int r = 0; r <= nrep; ++r)
+      if (j >= cnt[r]) mbar_arrive(b);
+    wait_bar_drain(b, (j / STAGES) & 1, DRAIN_LIMIT);
+  }
+}
+// A gather warp's arrival for stage slot s: local in the leader, relaxed
+// cluster-scope from the peer.
+__device__ __forceinline__ void gathered_arrive(const PairSmem& m, uint32_t full_l, bool leader,
+                                                int s) {
+  if (leader)
+    mbar_arrive(m.full + 8 * s);
+  else
+    mbar_arrive_cluster_relaxed(full_l + 8 * s);
 }
 static_assert(LAG < kRowsStages && LAG < kDwStages, "gather lag must be below the ring depth");
 
 // Barrier set-up, TMEM allocation on both CTAs, cluster-wide handshake.
+// full_count: the arrivals of full[s] per phase; pdone_count: the
+// producers that report at teardown besides the leader's TMA thread.
 template <int STAGES>
-__device__ __forceinline__ uint32_t pair_setup(const PairSmem& m, uint32_t full_count, int warp,
-                                               int epi_warps, int ring_consumers = 0) {
+__device__ __forceinline__ uint32_t pair_setup(const PairSmem& m, uint32_t full_count,
+                                               uint32_t pdone_count, int warp, int epi_warps,
+                                               int ring_consumers = 0) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(m.full + 8 * s, full_count);
       mbar_init(m.empty + 8 * s, 1);
-      mbar_init(m.gathered + 8 * s, 4);  // one arrival per gather warp of this CTA
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(m.acc_full + 8 * a, 1);
       mbar_init(m.acc_empty + 8 * a, 2 * epi_warps);  // one arrival per epilogue warp
     }
     mbar_init(m.drain, 1);
+    mbar_init(m.pdone, pdone_count);
     for (int r = 0; ring_consumers > 0 && r < TR; ++r) {
       mbar_init(m.tfull + 8 * r, 1);                   // the scheduler's arrival
       mbar_init(m.tempty + 8 * r, ring_consumers);     // every consumer of both CTAs
@@ -234,7 +284,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
     tma_prefetch_desc(&tmap_b);
   }
   pdl_trigger();
-  const uint32_t tmem_base = pair_setup<STAGES>(m, GATHER ? 2 : 1, warp, EPW);
+  // full: the two TMA threads' expect-tx arrivals and one per gather warp of
+  // both CTAs
+  const uint32_t tmem_base =
+      pair_setup<STAGES>(m, GATHER ? 10 : 2, GATHER ? kIssuedSlots : 1, warp, EPW);
   pdl_wait();  // the inputs may be the previous kernel's outputs
   const uint32_t full_l = mapa_shared(m.full, 0);           // leader's full[0]
   const uint32_t acc_empty_l = mapa_shared(m.acc_empty, 0);  // leader's acc_empty[0]
@@ -306,7 +359,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
             cp_async_wait<LAG>();
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(m.gathered + 8 * ((it - LAG) % STAGES));
+            if (lane == 0) gathered_arrive(m, full_l, leader, (it - LAG) % STAGES);
           }
           ++it;
         }
@@ -315,14 +368,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0)
-        for (int j = std::max(0, it - LAG); j < it; ++j) mbar_arrive(m.gathered + 8 * (j % STAGES));
+        for (int j = std::max(0, it - LAG); j < it; ++j) gathered_arrive(m, full_l, leader, j % STAGES);
+      if (lane == 0) report_issued(m, 1 + 4 * static_cast<int>(rank) + (warp - 6), it);
     }
   } else if (warp == 5) {
     // ------------------------------------------------ TMA: B half (+ A half in bare mode)
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      constexpr uint32_t TX = 2 * (B_STAGE + (GATHER ? 0 : A_STAGE));  // both CTAs
+      constexpr uint32_t TX = B_STAGE + (GATHER ? 0 : A_STAGE);  // this CTA's bytes
       for (int wi = 0, tau = pair; ok && more(wi, tau); ++wi, tau += npairs) {
         const WorkItem w = item(wi, tau);
         const Tile t = decode_tile(w.tau, p.tile_start, p.start, p.E, PBM);
@@ -334,6 +388,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
             break;
           }
           const uint32_t fb = full_l + 8 * s;
+          // the leader announces its bytes first; the peer issues its copies
+          // first and announces them after (a remote arrival would delay
+          // them; the phase cannot complete before that arrival anyway)
           if (leader) mbar_arrive_expect_tx(m.full + 8 * s, TX);
           if (!GATHER)
             tma_load_2d_cg2(m.sA + s * A_STAGE, &tmap_a, fb, kb * BK,
@@ -360,25 +417,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
             for (int j = 0; j < CBN / 64; ++j)
               tma_load_3d_cg2(dB + j * CHUNK, &tmap_b, fb, n0 + 64 * j, kb * BK, t.e);
           }
+          if (!leader) mbar_arrive_expect_tx_cluster(fb, TX);
           ++it;
         }
       }
-      if (leader)
-        for (int j = std::max(0, it - STAGES); j < it; ++j)
-          wait_bar_drain(m.full + 8 * (j % STAGES), (j / STAGES) & 1, DRAIN_LIMIT);
+      pair_drain<STAGES>(m, leader, GATHER, it);  // every copy lands before either CTA exits
     }
   } else if (warp == 4) {
-    // ------------------------------------------------ MMA issue (leader) / relay (peer)
-    if (!leader && GATHER && lane == 0) {
-      int it = 0;
-      bool ok = true;
-      for (int wi = 0, tau = pair; ok && more(wi, tau); ++wi, tau += npairs)
-        for (int kb = 0; kb < nkb; ++kb, ++it)
-          if (!relay_stage<STAGES>(m, full_l, it, wc)) {
-            ok = false;
-            break;
-          }
-    }
+    // ------------------------------------------------ MMA issue (leader)
     if (leader && lane == 0) {
       constexpr uint32_t IDESC =
           F8 ? idesc_e4m3_f32(PBM, PBN, false, false) : idesc_bf16_f32(PBM, PBN, false, B_MN);
@@ -396,8 +442,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
         for (int kb = 0; kb < nkb; ++kb) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!wait_bar(m.full + 8 * s, ph, wc) ||
-              (GATHER && !wait_bar(m.gathered + 8 * s, ph, wc))) {
+          if (!wait_bar(m.full + 8 * s, ph, wc)) {
             ok = false;
             break;
           }
@@ -822,7 +867,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
   constexpr bool dyn = DYN;
   // ring consumers per slot: 4 gather warps, the TMA thread, the MMA or
   // relay thread and 4 epilogue warps, in each CTA
-  const uint32_t tmem_base = pair_setup<STAGES>(m, 2, warp, 4, dyn ? 2 * 10 : 0);
+  // full: the two TMA threads' expect-tx arrivals and one per gather warp of
+  // both CTAs
+  const uint32_t tmem_base = pair_setup<STAGES>(m, 10, kIssuedSlots, warp, 4, dyn ? 2 * 10 : 0);
   pdl_wait();  // the inputs may be the previous kernel's outputs
   const uint32_t full_l = mapa_shared(m.full, 0);
   const uint32_t acc_empty_l = mapa_shared(m.acc_empty, 0);
@@ -1003,7 +1050,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
         cp_async_wait<LAG>();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(m.gathered + 8 * ((it - LAG) % STAGES));
+        if (lane == 0) gathered_arrive(m, full_l, leader, (it - LAG) % STAGES);
       }
       ++it;
       step(cur);
@@ -1017,7 +1064,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0)
-      for (int j = std::max(0, it - LAG); j < it; ++j) mbar_arrive(m.gathered + 8 * (j % STAGES));
+      for (int j = std::max(0, it - LAG); j < it; ++j) gathered_arrive(m, full_l, leader, j % STAGES);
+    if (lane == 0) report_issued(m, 1 + 4 * static_cast<int>(rank) + (warp - 6), it);
   } else if (warp == 5) {
     // ------------------------------------------------ scaled dY by TMA
     if (lane == 0) {
@@ -1034,38 +1082,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(m.full + 8 * s, 2 * B_STAGE);
+          const uint32_t fb = full_l + 8 * s;
+          // this CTA's bytes: the leader announces them first, the peer after
+          // its copies (as in the row kernels)
+          if (leader) mbar_arrive_expect_tx(m.full + 8 * s, B_STAGE);
           const uint32_t dB = m.sB + s * B_STAGE;
           if (p.b_merged) {
             // both 64-wide chunks of this CTA's n columns in one box
-            tma_load_3d_cg2(dB, &tmap_dyw, full_l + 8 * s, 0, ps + (t.kb0 + kb) * BK, n0 / 64);
+            tma_load_3d_cg2(dB, &tmap_dyw, fb, 0, ps + (t.kb0 + kb) * BK, n0 / 64);
           } else {
 #pragma unroll
             for (int j = 0; j < CBN / 64; ++j)
-              tma_load_2d_cg2(dB + j * CHUNK, &tmap_dyw, full_l + 8 * s, n0 + 64 * j,
-                              ps + (t.kb0 + kb) * BK);
+              tma_load_2d_cg2(dB + j * CHUNK, &tmap_dyw, fb, n0 + 64 * j, ps + (t.kb0 + kb) * BK);
           }
+          if (!leader) mbar_arrive_expect_tx_cluster(fb, B_STAGE);
           ++it;
         }
       }
-      if (leader)
-        for (int j = std::max(0, it - STAGES); j < it; ++j)
-          wait_bar_drain(m.full + 8 * (j % STAGES), (j / STAGES) & 1, DRAIN_LIMIT);
+      pair_drain<STAGES>(m, leader, true, it);  // every copy lands before either CTA exits
     }
   } else if (warp == 4) {
-    // ------------------------------------------------ MMA issue (leader) / relay (peer)
-    if (!leader && lane == 0) {
-      int it = 0;
-      bool ok = true;
-      for (int i = 0, tau = seq1(0); ok && tau < total; tau = seq1(++i)) {
-        const DwTile t = dw_tile(tau);
-        for (int kb = 0; kb < t.nkb; ++kb, ++it)
-          if (!relay_stage<STAGES>(m, full_l, it, wc)) {
-            ok = false;
-            break;
-          }
+    // ------------------------------------------------ MMA issue (leader)
+    // (with the dynamic schedule the peer's thread still takes every tile id
+    // off the ring, which counts one consumer per role and CTA)
+    if (!leader && lane == 0 && dyn)
+      for (int i = 0, tau = seq1(0); tau < total; tau = seq1(++i)) {
       }
-    }
     if (leader && lane == 0) {
       constexpr uint32_t IDESC = idesc_bf16_f32(PBM, PBN, true, true);
       int it = 0, tcount = 0;
@@ -1081,7 +1123,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DYN ? DW_THREADS : N
         for (int kb = 0; kb < t.nkb; ++kb) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!wait_bar(m.full + 8 * s, ph, wc) || !wait_bar(m.gathered + 8 * s, ph, wc)) {
+          if (!wait_bar(m.full + 8 * s, ph, wc)) {
             ok = false;
             break;
           }
