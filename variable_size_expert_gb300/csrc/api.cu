@@ -65,14 +65,14 @@ int dw_split_max() {
 
 // CTA pairs the backward gives dX when it runs dX and dW side by side (the
 // rest go to dW); 0 runs them one after the other.  MGG_BWD_SPLIT overrides:
-// a share in (0, 1), or 0.  Otherwise the split balances the two GEMMs'
-// estimated makespans on P pairs: dX has about (S/256 + E/2) row blocks x
-// ceil(K/256) tiles of N/64 contraction steps, dW E x ceil(K/256) x
-// ceil(N/256) tiles of about S/E/64 steps, each dW step measured about 1.15x
-// a dX step (its output stores).  (The estimate leaves out dW's contraction
-// split: counting it moved pairs from dX to dW at equal estimated cost and
-// made a K = N = 512 backward call slower, 63.9 -> 68.0 us; the prep still
-// splits for the pairs dW gets.)
+// a share in (0, 1), or 0.  Otherwise dX gets 48% of the pairs, but no more
+// pairs than it has tiles, and dW no more than its tiles.  The two GEMMs do
+// the same FLOPs; sweeping the share measured the backward call flat between
+// 0.47 and 0.50 on the top-2 workload (143-144 us) and best at 0.47-0.50 on
+// the skewed E=64, k=8 one (484-489 us against 513 at 0.53); a makespan
+// model from the tiles' contraction lengths picked 0.53 there, since the two
+// kernels share the L2 and DRAM side by side and run neither at their
+// whole-GPU rates.
 int bwd_dx_pairs(int P, long long S, int E, int K, int N) {
   if (const char* s = getenv("MGG_BWD_SPLIT")) {
     const double v = atof(s);
@@ -83,20 +83,10 @@ int bwd_dx_pairs(int P, long long S, int E, int K, int N) {
   const long long tk = cdiv(K, 256), tn = cdiv(N, 256);
   const long long t_dx = (cdiv(static_cast<int>(std::min<long long>(S, 1LL << 30)), 256) + E / 2) * tk;
   const long long t_dw = static_cast<long long>(E) * tk * tn;
-  const double c_dx = static_cast<double>(N);
-  const double c_dw = 1.15 * static_cast<double>(S) / E;
-  int best = 0;
-  double best_cost = 0.0;
-  for (int a = 1; a < P; ++a) {
-    const double dx = static_cast<double>((t_dx + a - 1) / a) * c_dx;
-    const double dw = static_cast<double>((t_dw + (P - a) - 1) / (P - a)) * c_dw;
-    const double cost = std::max(dx, dw);
-    if (best == 0 || cost < best_cost) {
-      best = a;
-      best_cost = cost;
-    }
-  }
-  return best;
+  long long a = static_cast<long long>(0.48 * P + 0.5);
+  a = std::max(a, static_cast<long long>(P) - t_dw);  // dW cannot use more pairs than tiles
+  a = std::min(a, t_dx);                              // nor dX
+  return static_cast<int>(std::min<long long>(P - 1, std::max<long long>(1, a)));
 }
 
 // CTA pairs of the gated FFN backward's main-stream GEMMs in its two
