@@ -71,7 +71,16 @@ constexpr int rows_epi_warps(int mode) {
 }
 constexpr int rows_threads(int mode) { return rows_epi_warps(mode) == 8 ? 448 : NUM_THREADS; }
 constexpr int TMEM_COLS = 2 * PBN;
-constexpr int kRowsEpi = 16 * 1024;    // epilogue staging: 4 warps x 32 x 32 f32 or 8 x 32 x 16
+// Columns per staged epilogue block: the dX GEMM's eight warps stage 32
+// columns each (32 KB of staging; against 16-column blocks in 16 KB its x
+// reads for the d(routing weight) dot cover 64 instead of 32 bytes of a row
+// per instruction and its accumulator loads are full width), the gated
+// backward's eight warps 16 (their saved gate and up values would not fit
+// in registers twice over), four warps 32.
+constexpr int rows_epi_cols(int mode) {
+  return rows_epi_warps(mode) == 8 && mode != kModeFusedDtopk ? 16 : 32;
+}
+constexpr int rows_epi_bytes(int mode) { return rows_epi_warps(mode) * 32 * rows_epi_cols(mode) * 4; }
 constexpr int DW_EPI_BUF = 32 * 32 * 4;  // one warp's 32 (n) x 32 (k) f32 block
 constexpr int kDwEpi = 4 * 2 * DW_EPI_BUF;  // double-buffered per epilogue warp
 constexpr int kBarBytes = 640;
@@ -80,7 +89,7 @@ template <int STAGES, int EPI_BYTES>
 constexpr size_t smem_bytes() {
   return 1024 + static_cast<size_t>(STAGES) * (A_STAGE + B_STAGE) + EPI_BYTES + kBarBytes;
 }
-static_assert(smem_bytes<kRowsStages, kRowsEpi>() <= 232448 &&
+static_assert(smem_bytes<kRowsStages, rows_epi_bytes(kModeFusedDtopk)>() <= 232448 &&
                   smem_bytes<kDwStages, kDwEpi>() <= 232448,
               "shared memory per block");
 constexpr long long DRAIN_LIMIT = 200000000LL;
@@ -264,14 +273,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
   static_assert(!F8 || ((MODE == kModeFused || MODE == kModeBare) && !B_MN),
                 "e4m3 operands: fused and bare modes, K-major");
   constexpr int EPW = rows_epi_warps(MODE);  // epilogue warps
-  constexpr int CW = EPW == 8 ? 16 : 32;     // columns per staged block
+  constexpr int CW = rows_epi_cols(MODE);    // columns per staged block
   constexpr int LPR = CW / 4;                // lanes per staged row after the transpose
   constexpr int RSTEP = 32 / LPR;            // rows per store instruction
-  static_assert(EPW * 32 * CW * 4 == kRowsEpi, "staging area");
+  constexpr int EPI_BYTES = rows_epi_bytes(MODE);  // staging area
   static_assert(!GATEUP || CW == 32, "the gate/up epilogue stages 32-column blocks");
   extern __shared__ uint8_t smem_raw[];
   constexpr int STAGES = kRowsStages;
-  const PairSmem m = carve<STAGES, kRowsEpi>(smem_raw);
+  const PairSmem m = carve<STAGES, EPI_BYTES>(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -1274,7 +1283,7 @@ cudaError_t launch_rows_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
                                cudaStream_t st) {
   auto kern = rows_pair_kernel<MODE, B_MN, F8>;
   static bool done[64] = {};
-  constexpr size_t smem = smem_bytes<kRowsStages, kRowsEpi>();
+  constexpr size_t smem = smem_bytes<kRowsStages, rows_epi_bytes(MODE)>();
   cudaError_t e = prepare(kern, smem, done);
   if (e != cudaSuccess) return e;
   constexpr int threads = rows_threads(MODE);
