@@ -351,6 +351,9 @@ TRAFFIC_NOTES = {
                     "write-back L2 when the kernel ends"),
     "fwd_gather_scatter_gemm": ("includes reading back y (33.6 MB): the router zeroes y and the "
                                 "epilogue's atomic adds fetch those lines again"),
+    "bwd_dx_dtopk_gemm": ("includes reading back dx (33.6 MB: the backward prep zeroes dx and the "
+                          "epilogue's atomic adds fetch those lines again) and x (16.8 MB) for the "
+                          "d(routing weight) dot"),
 }
 
 
