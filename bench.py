@@ -497,7 +497,10 @@ def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush, peak_tf):
                       "tflops": round(2.0 * 256 * 128 * 96 / (be["us_per_call"] * 1e-6) / 1e12, 3)},
         "3_fwd_skew": {"ms": fs["ms"], "tflops": fs["tflops"], "gemm_ms": fs["gemm_ms"],
                        "gemm_frac": round(fs["gemm_tflops"] / peak_tf, 4),
-                       "useful_rows": fs["useful_row_fraction"]},
+                       "useful_rows": fs["useful_row_fraction"],
+                       "tile_pick": fs["row_tile"]["device_pick"],
+                       "tflops_256_128": [fs["row_tile"]["gemm_tflops_256_pair"],
+                                          fs["row_tile"]["gemm_tflops_128_cta"]]},
         "4_bwd_top2": {"ms": bs["side_by_side_ms"],
                        "tflops": round(bwd_fl / (bs["side_by_side_ms"] * 1e-3) / 1e12, 1),
                        "frac": round(bwd_fl / (bs["side_by_side_ms"] * 1e-3) / 1e12 / peak_tf, 4)},
@@ -711,6 +714,25 @@ def _run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
     counts = r.counts.cpu().numpy()
     bm, bn, _ = mgg.tile_config(L.MGG_OP_FORWARD)
     tiles = int(sum(-(-int(m) // bm) for m in counts)) * (-(-N // bn))
+    # each row-tile height forced, and the one the device picks per call
+    by_tile = {}
+    for tile in ("256", "128"):
+        with _Env(MGG_ROW_TILE=tile):
+            for _ in range(3):
+                mgg.moe_forward(*args_, out=y, routing=r)
+            tk = []
+            for _ in range(10):
+                flush.zero_()
+                lib.mgg_set_kernel_events(h, 1)
+                mgg.moe_forward(*args_, out=y, routing=r)
+                lib.mgg_set_kernel_events(None, 0)
+                torch.cuda.synchronize()
+                tk.append(ev.ms(0))
+        by_tile[tile] = round(fl / (statistics.mean(tk) * 1e-3) / 1e12, 1)
+    pick = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.mgg_debug_row_tile(r.start.data_ptr(), E, N, pick.data_ptr(),
+                           torch.cuda.current_stream().cuda_stream)
+    useful128 = float(counts.sum()) / (128 * sum(-(-int(m) // 128) for m in counts))
     res["fwd_skew"] = {
         "workload": "fused forward, Zipf(1.2) routing: T=4096, K=2048, N=1536, E=64, k=8; seed 0",
         "ms": round(statistics.mean(t_all), 4), "gemm_ms": round(statistics.mean(t_k), 4),
@@ -718,7 +740,11 @@ def _run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
         "gemm_tflops": round(fl / (statistics.mean(t_k) * 1e-3) / 1e12, 1),
         "tile": [bm, bn],
         "useful_row_fraction": round(float(counts.sum()) / (bm * sum(-(-int(m) // bm) for m in counts)), 4),
-        "tiles": tiles, "count_min": int(counts.min()), "count_max": int(counts.max())}
+        "tiles": tiles, "count_min": int(counts.min()), "count_max": int(counts.max()),
+        "row_tile": {"gemm_tflops_256_pair": by_tile["256"], "gemm_tflops_128_cta": by_tile["128"],
+                     "useful_rows_128": round(useful128, 4),
+                     "device_pick": 128 if int(pick.item()) else 256,
+                     "default": "pair tiles (both kernels and the device's pick only when T*k < 256*E)"}}
     # skewed backward (same inputs + dy): dW's tile costs follow the expert
     # row counts, the case its longest-first snake schedule is for
     dys = torch.from_numpy(np.random.default_rng(1).standard_normal((T, N), dtype=np.float32)).to(dev)

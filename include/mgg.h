@@ -449,6 +449,27 @@ mgg_status mgg_debug_tile_schedule(const mgg_routing* routing, int E, int N, mgg
                                    int max_tiles, int32_t* out, void* stream);
 
 /*
+ * The per-call row-tile choice of the fused forward and the bare grouped GEMM
+ * ("Grouped GEMM for MoE, in depth", §Worked example: under skew a smaller
+ * row tile keeps more of a tile's rows useful; libraries pick one of several
+ * tile configurations per call from the observed counts), evaluated on the
+ * device exactly as those calls evaluate it when both tile kernels run:
+ *   start  [E+1] int32 device  exclusive scan of the expert row counts
+ *                              (mgg_routing.start)
+ *   N                          output columns
+ *   out    [1] int32 device    1: 128-row tiles on single CTAs chosen,
+ *                              0: 256-row tiles on CTA pairs
+ * The choice compares the two tilings' rounds of tiles over their workers
+ * (76 CTA pairs, 152 CTAs on GB300), a round of 128-row tiles counted as 6/5
+ * of a round of pair tiles.  MGG_ROW_TILE=256 / 128 / auto in the
+ * environment forces the forward's and the bare GEMM's tile height; by
+ * default they make this choice when T*k < 256*E and use the pair tiles
+ * otherwise.  Stream-ordered.  Errors: MGG_ERR_INVALID_ARG (null, E < 1,
+ * E > MGG_MAX_EXPERTS, N < 1), MGG_ERR_UNSUPPORTED_ARCH, MGG_ERR_CUDA.
+ */
+mgg_status mgg_debug_row_tile(const int32_t* start, int E, int N, int32_t* out, void* stream);
+
+/*
  * Test of the bounded wait every pipeline uses (failure detection without a
  * GPU fault): one thread waits, with the kernels' own wait helper and a limit
  * of limit_cycles SM clock cycles (1 .. 2^40), on an mbarrier that nothing

@@ -29,3 +29,30 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Achieved parity errors of the GPU tests: per bar, the number of
+    comparisons, the median and the worst (with its test)."""
+    try:
+        from tests.gpu_util import ACHIEVED
+    except Exception:
+        return
+    if not ACHIEVED:
+        return
+    import statistics
+    tr = terminalreporter
+    tr.write_sep("-", "achieved parity errors (bars: bf16 rel-Frobenius 1e-3, max-abs 2e-3; f32 1e-5)")
+    for bar in ("bf16", "f32"):
+        rows = [r for r in ACHIEVED if r[2] == bar]
+        if not rows:
+            continue
+        rfs = [r[3] for r in rows]
+        worst = max(rows, key=lambda r: r[3])
+        line = (f"{bar}: {len(rows)} comparisons, rel-Frobenius median {statistics.median(rfs):.2e}, "
+                f"worst {worst[3]:.2e} ({worst[0]} {worst[1]})")
+        mas = [r[4] for r in rows if r[4] is not None]
+        if mas:
+            wm = max((r for r in rows if r[4] is not None), key=lambda r: r[4])
+            line += f"; max-abs median {statistics.median(mas):.2e}, worst {wm[4]:.2e} ({wm[0]} {wm[1]})"
+        tr.write_line(line)

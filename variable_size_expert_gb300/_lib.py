@@ -48,7 +48,7 @@ EXPORTS = (
     "mgg_grouped_gemm", "mgg_moe_forward", "mgg_moe_backward", "mgg_debug_tile_schedule",
     "mgg_set_kernel_events", "mgg_route_noalloc", "mgg_moe_ffn_forward", "mgg_quantize_fp8",
     "mgg_grouped_gemm_fp8", "mgg_moe_forward_fp8", "mgg_moe_ffn_backward",
-    "mgg_debug_wait_timeout",
+    "mgg_debug_wait_timeout", "mgg_debug_row_tile",
 )
 
 
@@ -81,6 +81,7 @@ _SIGS = {
     "mgg_debug_tile_schedule": (_I, [_RP, _I, _I, _I, _I, _P, _P]),
     "mgg_set_kernel_events": (_I, [ctypes.POINTER(_P), _I]),
     "mgg_debug_wait_timeout": (_I, [_P, ctypes.c_longlong, _P]),
+    "mgg_debug_row_tile": (_I, [_P, _I, _I, _P, _P]),
     "mgg_route_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _RP, _P, _P]),
     "mgg_moe_ffn_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _RP,
                                  _P, _P, _SZ, _P]),

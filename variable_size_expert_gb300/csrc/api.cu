@@ -5,6 +5,7 @@
 #include <stdlib.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -61,6 +62,41 @@ int dw_split_max() {
     return v <= 1 ? 1 : std::min(v, kDwSplitMax);
   }
   return kDwSplitMax;
+}
+
+// Row-tile height of the fused forward and the bare grouped GEMM (bf16):
+// the 256-row tiles on CTA pairs, the 128-row tiles on single CTAs
+// (gemm_cta.cu), or both kernels launched with the choice made per call on
+// the device from the expert counts (choose_rows128; the kernel not chosen
+// exits at entry).  MGG_ROW_TILE=256 / 128 / auto forces one.  By default
+// the choice runs only where it can go to the 128-row tile: when the
+// average expert holds fewer than kRowTileAutoRows rows.  Above that the
+// padding of the experts' last row blocks is too small a share for the
+// 128-row tile to make up its cost (skewed E=64, k=8, 512 rows per expert
+// on average: 1182 TFLOP/s on pair tiles, 1100 on 128-row tiles, 1169 with
+// both launched and the pair tile picked), and the second launch only adds
+// its start-up.
+constexpr long long kRowTileAutoRows = 256;
+int row_tile_mode(long long S, int E) {
+  if (const char* v = getenv("MGG_ROW_TILE")) {
+    if (!strcmp(v, "128")) return kRowTileCta;
+    if (!strcmp(v, "auto")) return kRowTileAuto;
+    if (!strcmp(v, "256")) return kRowTilePair;
+  }
+  return S < kRowTileAutoRows * E ? kRowTileAuto : kRowTilePair;
+}
+
+// The row GEMM of the fused forward or the bare grouped GEMM on the row-tile
+// height `mode` picks.
+cudaError_t launch_rows_tiled(int mode_op, const CUtensorMap& ta, const CUtensorMap& tb,
+                              RowsParams p, long long S, cudaStream_t st) {
+  p.row_tile = row_tile_mode(S, p.E);
+  p.pair_workers = num_sms() / 2;
+  p.cta_workers = num_sms();
+  cudaError_t e = cudaSuccess;
+  if (p.row_tile != kRowTileCta) e = launch_rows_pair(mode_op, false, ta, tb, p, st);
+  if (e == cudaSuccess && p.row_tile != kRowTilePair) e = launch_rows_cta(mode_op, ta, tb, p, st);
+  return e;
 }
 
 // CTA pairs the backward gives dX when it runs dX and dW side by side (the
@@ -492,7 +528,8 @@ mgg_status mgg_grouped_gemm(const void* A, const void* W, float* C, mgg_dtype dt
   CUtensorMap tm, ta;
   if (!tmap_weights(&tm, W, E, N, K, kBK, kPairBN / 2)) return MGG_ERR_CUDA;
   if (!tmap_rows(&ta, A, rows_or_Mmax, K, kPairBM / 2)) return MGG_ERR_CUDA;
-  return from_cuda(timed(0, st, [&] { return launch_rows_pair(kModeBare, false, ta, tm, p, st); }));
+  return from_cuda(
+      timed(0, st, [&] { return launch_rows_tiled(kModeBare, ta, tm, p, rows_or_Mmax, st); }));
 }
 
 mgg_status mgg_moe_forward(const void* x, const void* W, const int32_t* expert_ids,
@@ -539,7 +576,9 @@ mgg_status mgg_moe_forward(const void* x, const void* W, const int32_t* expert_i
     }));
   CUtensorMap tm;
   if (!tmap_weights(&tm, W, E, N, K, kBK, kPairBN / 2)) return MGG_ERR_CUDA;
-  return from_cuda(timed(0, st, [&] { return launch_rows_pair(kModeFused, false, tm, tm, p, st); }));
+  return from_cuda(timed(0, st, [&] {
+    return launch_rows_tiled(kModeFused, tm, tm, p, static_cast<long long>(T) * k, st);
+  }));
 }
 
 mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
@@ -1109,6 +1148,13 @@ mgg_status mgg_debug_wait_timeout(int32_t* dev_status, long long limit_cycles, v
   mgg_status s = check_arch();
   if (s != MGG_OK) return s;
   return from_cuda(launch_wait_timeout(dev_status, limit_cycles, static_cast<cudaStream_t>(stream)));
+}
+
+mgg_status mgg_debug_row_tile(const int32_t* start, int E, int N, int32_t* out, void* stream) {
+  if (!start || !out || E < 1 || E > kMaxExperts || N < 1) return MGG_ERR_INVALID_ARG;
+  mgg_status s = check_arch();
+  if (s != MGG_OK) return s;
+  return from_cuda(launch_row_tile_choice(start, E, N, out, static_cast<cudaStream_t>(stream)));
 }
 
 mgg_status mgg_set_kernel_events(void* const* events, int n) {

@@ -98,6 +98,7 @@ constexpr long long DRAIN_LIMIT = 200000000LL;
 struct PairSmem {
   uint32_t sA, sB, sEpi, full, empty, acc_full, acc_empty, drain, pdone;
   uint32_t issued;               // producers' counts of issued stages (9 ints)
+  uint32_t choice;               // the per-call row-tile choice (int)
   uint32_t tfull, tempty, tids;  // dynamic tile ring: barriers and tile ids
   uint32_t* tmem_slot;
   volatile int* abort_flag;
@@ -126,6 +127,7 @@ __device__ __forceinline__ PairSmem carve(uint8_t* smem_raw) {
   m.tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar0 - base) + 8 * NUM_BARS);
   m.abort_flag = reinterpret_cast<volatile int*>(m.tmem_slot + 1);
   m.issued = bar0 + 8 * NUM_BARS + 8;
+  m.choice = bar0 + 8 * NUM_BARS + 44;
   m.tids = bar0 + 8 * NUM_BARS + 48;
   return m;
 }
@@ -302,7 +304,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
   const uint32_t acc_empty_l = mapa_shared(m.acc_empty, 0);  // leader's acc_empty[0]
 
   const WaitCtl wc{m.abort_flag, p.dev_status, p.wait_limit};
-  const int total = __ldg(p.tile_start + p.E);
+  int total = __ldg(p.tile_start + p.E);
+  if constexpr ((MODE == kModeFused || MODE == kModeBare) && !F8) {
+    // with the 128-row single-CTA kernel launched beside this one, both
+    // evaluate the per-call row-tile choice; the one not chosen does no work
+    if (p.row_tile == kRowTileAuto) {
+      if (warp == 0) {
+        const bool r128 = choose_rows128(p.start, p.E, cdiv(p.Nout, PBN), p.pair_workers,
+                                         p.cta_workers, kRow128CostNum, kRow128CostDen);
+        if (lane == 0) st_shared_s32(m.choice, r128 ? 1 : 0);
+      }
+      __syncthreads();
+      if (ld_shared_s32(m.choice)) total = 0;
+    }
+  }
   const int nkb = cdiv(p.Kc, BK);
   // The column halves of the last round pay off only where A arrives by TMA:
   // a half still needs all 256 gathered rows, and in the gather modes the

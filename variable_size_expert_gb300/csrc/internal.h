@@ -95,9 +95,22 @@ struct RowsParams {
   const float* gu;
   int ldgu;
   int max_pairs;               // cap on the persistent grid's CTA pairs (0: all that fit)
+  // Row-tile height (fused and bare modes, bf16): kRowTilePair runs the
+  // 256-row pair tiles only, kRowTileCta the 128-row single-CTA tiles only,
+  // kRowTileAuto launches both kernels and each evaluates choose_rows128 on
+  // the device; the one not chosen exits at entry.
+  int row_tile;
+  int pair_workers, cta_workers;  // the two kernels' grids (kRowTileAuto): 76 pairs, 152 CTAs
   int32_t* dev_status;
   long long wait_limit;
 };
+enum RowTile { kRowTilePair = 0, kRowTileAuto = 1, kRowTileCta = 2 };
+// Measured cost of a round of 128 x 256 single-CTA tiles relative to a
+// round of 256 x 256 pair tiles (each SM of a pair moves half the weight
+// bytes per FLOP of a single CTA): rnum / rden; 1.15 on the skewed forward
+// (E=64, k=8, Zipf 1.2: 15.6 against 13.6 us per round).
+constexpr int kRow128CostNum = 6;
+constexpr int kRow128CostDen = 5;
 
 struct DwParams {
   const void* x;               // [T, K]
@@ -180,6 +193,13 @@ cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* star
 cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_a,
                              const CUtensorMap& tmap_b, const RowsParams& p, cudaStream_t st,
                              bool f8 = false);
+// gemm_cta.cu (tcgen05, cta_group::1): 128-row tiles, kModeFused or
+// kModeBare; tmap_b is the weights' map with 128-row boxes (two per stage)
+cudaError_t launch_rows_cta(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                            const RowsParams& p, cudaStream_t st);
+// writes the device's per-call row-tile choice (1: 128-row tiles) to out[0]
+cudaError_t launch_row_tile_choice(const int32_t* start, int E, int N, int32_t* out,
+                                   cudaStream_t st);
 // tmap_dw: dW [E][N][K] f32 as a 3-D map, box {32, 32, 1}, no swizzle.
 cudaError_t launch_dw_pair(const CUtensorMap& tmap_dyw, const CUtensorMap& tmap_dw,
                            const DwParams& p, cudaStream_t st);

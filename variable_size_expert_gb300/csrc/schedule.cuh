@@ -43,6 +43,36 @@ __device__ __forceinline__ Tile decode_tile(int tau, const int32_t* __restrict__
   return t;
 }
 
+// Row-tile height chosen per call on the device from the expert row counts
+// ("Grouped GEMM for MoE, in depth", §Worked example: under skew a smaller
+// row tile wastes fewer padded rows, and libraries pick one of several tile
+// configurations per call from the observed count distribution).  The two
+// candidates tile the output 256 columns wide: 256-row tiles on `pairs` CTA
+// pairs, or 128-row tiles on `ctas` single CTAs.  A candidate's makespan is
+// its number of rounds of tiles over its workers; a round of 128-row tiles
+// costs rnum / rden rounds of pair tiles (measured, see the caller).  The
+// 128-row tile is chosen only when its makespan is strictly shorter.  One
+// warp evaluates it from the start offsets (start[e + 1] - start[e] = m_e),
+// identically in both kernels, which read the same offsets.
+__device__ __forceinline__ bool choose_rows128(const int32_t* start, int E, int tiles_n,
+                                               int pairs, int ctas, int rnum, int rden) {
+  const int lane = threadIdx.x & 31;
+  long long rb256 = 0, rb128 = 0;
+  for (int e = lane; e < E; e += 32) {
+    const int m = ld_dep(start + e + 1) - ld_dep(start + e);
+    rb256 += (m + 255) / 256;
+    rb128 += (m + 127) / 128;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    rb256 += __shfl_xor_sync(0xffffffffu, rb256, o);
+    rb128 += __shfl_xor_sync(0xffffffffu, rb128, o);
+  }
+  const long long r256 = (rb256 * tiles_n + pairs - 1) / pairs;
+  const long long r128 = (rb128 * tiles_n + ctas - 1) / ctas;
+  return r128 * rnum < r256 * rden;
+}
+
 // The work of persistent worker w (of W) over `total` tiles.  Whole tiles go
 // round-robin.  When the last round would leave more than half of the
 // workers idle (0 < total mod W <= W/2), its tiles are cut instead into two
