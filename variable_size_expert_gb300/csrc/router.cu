@@ -297,14 +297,18 @@ __global__ void __launch_bounds__(1024)
       for (int v = 0; v < 32; ++v) m += wc[v][e];
       hist[b * E + e] = m;
     }
-  } else {
+  }
+  grid.sync();  // every block's totals are published
+  if (!router) {
+    // the other blocks zero y after the barrier, so the routing blocks'
+    // second pass runs beside the zeroing instead of after it (only the
+    // kernel's completion orders y before the GEMM's atomic adds)
     const long long stride = static_cast<long long>(gridDim.x - nb) * blockDim.x;
     for (long long i = static_cast<long long>(b - nb) * blockDim.x + threadIdx.x; i < nzero4;
          i += stride)
       zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
   }
-  grid.sync();  // every block's totals are published
-  if (!router) return;
   const int e = threadIdx.x;
   int m = 0, before = 0;
   if (e < E)
