@@ -30,7 +30,7 @@ __all__ = [
     "moe_loss", "rel_frobenius", "max_abs_ratio", "silu", "moe_ffn_forward", "moe_ffn_backward",
     "moe_ffn_loss", "moe_ffn_backward_rows", "moe_ffn_backward_dw_rows",
     "E4M3_MAX", "e4m3_decode", "e4m3_encode", "quantize_fp8_rows", "grouped_gemm_fp8",
-    "moe_forward_fp8", "masked_grouped_gemm_fp8",
+    "moe_forward_fp8", "masked_grouped_gemm_fp8", "quantize_fp8_cols", "moe_backward_dx_fp8",
 ]
 
 
@@ -611,6 +611,56 @@ def quantize_fp8_rows(v):
     scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
     q = e4m3_encode(v32 / scale[:, None])
     return q, scale
+
+
+def quantize_fp8_cols(W):
+    """Per-column e4m3 quantisation of a stack of matrices W [E, N, K]:
+    (codes [E, K, N] uint8, scale [E, K] float32), the codes transposed.
+
+    Column k of W_e (its N values) is quantised like one row of
+    ``quantize_fp8_rows``: s_ek = fl32(amax_n |W_enk| / 448) (1 for an
+    all-zero column) and q_ekn = e4m3(fl32(W_enk / s_ek)).  Stored
+    transposed, row (e, k) holds the contraction over n of the backward's
+    dX = dy W_e contiguously, and its scale varies only with the output
+    column k, so it factors out of that contraction.
+    """
+    W32 = np.asarray(W, dtype=np.float32)
+    E, N, K = W32.shape
+    q, s = quantize_fp8_rows(np.ascontiguousarray(W32.transpose(0, 2, 1)).reshape(E * K, N))
+    return q.reshape(E, K, N), s.reshape(E, K)
+
+
+def moe_backward_dx_fp8(dyq, dy_scale, Wtq, wt_scale, x, expert_ids, topk_weights,
+                        tokens=None):
+    """dx and d(routing weight) of ``moe_backward`` on e4m3 operands whose
+    scales factor out of the dX contraction over n: dy quantised per token
+    (dyq [T, N], dy_scale [T]) and W quantised per (expert, column k)
+    (``quantize_fp8_cols``: Wtq [E, K, N], wt_scale [E, K]).  With
+      G[t, j, k] = dy_scale[t] * wt_scale[e, k] * sum_n dec(dyq[t, n]) dec(Wtq[e, k, n]),
+      e = ids[t, j]:
+      dx[t, k]    = sum_j w[t, j] G[t, j, k]
+      dtopk[t, j] = sum_k x[t, k] G[t, j, k]   (= <dy_deq[t], x[t] W_deq_e^T>)
+    x is used as given (bfloat16 values).  ``tokens`` restricts the rows.
+    Returns (dx [T or len(tokens), K], dtopk [.., k]).
+    """
+    ids = np.asarray(expert_ids)
+    w = np.asarray(topk_weights, dtype=np.float64)
+    x = np.asarray(x, dtype=np.float64)
+    dy_scale = np.asarray(dy_scale, dtype=np.float64)
+    wt_scale = np.asarray(wt_scale, dtype=np.float64)
+    rows = np.arange(ids.shape[0]) if tokens is None else np.asarray(tokens)
+    k = ids.shape[1]
+    K = Wtq.shape[1]
+    D = e4m3_decode(dyq[rows])
+    dx = np.zeros((len(rows), K))
+    dtopk = np.zeros((len(rows), k))
+    for j in range(k):
+        for e in np.unique(ids[rows, j]):
+            sel = np.nonzero(ids[rows, j] == e)[0]
+            G = (D[sel] @ e4m3_decode(Wtq[e]).T) * dy_scale[rows[sel], None] * wt_scale[e][None, :]
+            dx[sel] += w[rows[sel], j][:, None] * G
+            dtopk[sel, j] = np.sum(x[rows[sel]] * G, axis=1)
+    return dx, dtopk
 
 
 def grouped_gemm_fp8(Aq, a_scale, Wq, w_scale, end_offs) -> np.ndarray:

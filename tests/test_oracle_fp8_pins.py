@@ -249,3 +249,119 @@ def test_fp8_planted_mistakes_are_caught():
         return y
     for bad in (fwd_scale_by_column, fwd_w_scale_of_expert0):
         assert not np.allclose(bad(xq, sx, Wq, sw), good, rtol=1e-9)
+
+
+# ------------------------------------------------------------------ backward dX
+def _bwd_fp8_operands(T, K, N, E, seed):
+    rng = np.random.default_rng(seed)
+    # each dy row peaks at +-448 * 2^s, so its scale is the power of two 2^s
+    # and the dequantised dy is exact in float32 (the reduction below takes
+    # dy in float32, as the GPU's bf16 path does)
+    p2 = np.exp2(rng.integers(-6, 3, size=T)).astype(np.float32)
+    dy = np.clip(rng.standard_normal((T, N)) * 120.0, -440.0, 440.0).astype(np.float32)
+    peak = rng.integers(0, N, size=T)
+    dy[np.arange(T), peak] = np.where(rng.random(T) < 0.5, -448.0, 448.0)
+    dyq, sdy = O.quantize_fp8_rows(dy * p2[:, None])
+    assert np.array_equal(sdy, p2)
+    W = (rng.standard_normal((E, N, K)) / np.sqrt(N)).astype(np.float32)
+    Wtq, swt = O.quantize_fp8_cols(W)
+    x = O.bf16_round(rng.standard_normal((T, K)).astype(np.float32))
+    return dyq, sdy, Wtq, swt, x
+
+
+def _w_deq(Wtq, swt):
+    """W [E, N, K] from the transposed column codes: W[e, n, k] = dec(Wtq[e, k, n]) swt[e, k]."""
+    return (O.e4m3_decode(Wtq) * np.asarray(swt, dtype=np.float64)[..., None]).transpose(0, 2, 1)
+
+
+def test_quantize_cols_is_the_row_quantiser_on_columns():
+    rng = np.random.default_rng(11)
+    W = rng.standard_normal((3, 7, 5)).astype(np.float32) * np.array([1, 1e-3, 5e2])[:, None, None].astype(np.float32)
+    W[1, :, 2] = 0.0                               # an all-zero column
+    q, s = O.quantize_fp8_cols(W)
+    assert q.shape == (3, 5, 7) and s.shape == (3, 5)
+    for e in range(3):
+        for kk in range(5):
+            col = W[e, :, kk]
+            amax = np.float32(np.abs(col).max())
+            want_s = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+            assert s[e, kk] == want_s
+            assert np.array_equal(q[e, kk], _torch_encode(col / want_s))
+            if amax > 0:                           # the column reaches the code range's top
+                assert np.abs(O.e4m3_decode(q[e, kk])).max() == 448.0
+    assert np.array_equal(q[1, 2], np.zeros(7, dtype=np.uint8)) and s[1, 2] == 1.0
+
+
+@pytest.mark.parametrize("routing", ["uniform", "random"])
+def test_moe_backward_dx_fp8_reduces_to_moe_backward(routing):
+    """On the dequantised operands the FP8 dX and d(routing weight) equal the
+    (pinned) unrounded backward: dx = sum_j w dy W_e, dtopk = <dy, x W_e^T>."""
+    T, K, N, E, k = 10, 12, 16, 3, 2
+    dyq, sdy, Wtq, swt, x = _bwd_fp8_operands(T, K, N, E, seed=12)
+    p = workloads.moe_problem(T=T, K=K, N=N, E=E, k=k, seed=12, routing=routing)
+    ids, w = p["expert_ids"].numpy(), p["topk_weights"].numpy()
+    dx, dt = O.moe_backward_dx_fp8(dyq, sdy, Wtq, swt, x, ids, w)
+    dy_deq = O.e4m3_decode(dyq) * sdy[:, None].astype(np.float64)
+    rdx, _, rdt = O.moe_backward(dy_deq, x, _w_deq(Wtq, swt), ids, w, bf16_operands=False)
+    np.testing.assert_allclose(dx, rdx, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dt, rdt, rtol=1e-11, atol=1e-12)
+    tok = np.array([1, 4, 9])
+    sdx, sdt = O.moe_backward_dx_fp8(dyq, sdy, Wtq, swt, x, ids, w, tokens=tok)
+    np.testing.assert_allclose(sdx, dx[tok], rtol=1e-14, atol=0)
+    np.testing.assert_allclose(sdt, dt[tok], rtol=1e-14, atol=0)
+
+
+def test_moe_backward_dx_fp8_bruteforce():
+    T, K, N, E = 3, 4, 5, 2
+    dyq, sdy, Wtq, swt, x = _bwd_fp8_operands(T, K, N, E, seed=13)
+    ids = np.array([[0, 1], [1, 1], [0, 0]], dtype=np.int32)  # repeated experts included
+    w = np.array([[0.5, 0.25], [0.75, 1.0], [0.125, 0.5]], dtype=np.float32)
+    dx, dt = O.moe_backward_dx_fp8(dyq, sdy, Wtq, swt, x, ids, w)
+    F = lambda v: Fraction(float(v))
+    for t in range(T):
+        for j in range(2):
+            e = ids[t, j]
+            G = [sum(F(O.e4m3_decode(dyq[t, n])) * F(O.e4m3_decode(Wtq[e, kk, n])) for n in range(N))
+                 * F(sdy[t]) * F(swt[e, kk]) for kk in range(K)]
+            d = sum(F(x[t, kk]) * G[kk] for kk in range(K))
+            assert abs(dt[t, j] - float(d)) <= 1e-14 * max(1.0, abs(float(d)))
+        for kk in range(K):
+            acc = Fraction(0)
+            for j in range(2):
+                e = ids[t, j]
+                acc += F(w[t, j]) * sum(F(O.e4m3_decode(dyq[t, n])) * F(O.e4m3_decode(Wtq[e, kk, n]))
+                                        for n in range(N)) * F(sdy[t]) * F(swt[e, kk])
+            assert abs(dx[t, kk] - float(acc)) <= 1e-14 * max(1.0, abs(float(acc)))
+
+
+def test_fp8_backward_planted_mistakes_are_caught():
+    """Copies of the FP8 dX step with one plausible mistake each fail the
+    reduction pin."""
+    T, K, N, E = 6, 8, 8, 3
+    dyq, sdy, Wtq, swt, x = _bwd_fp8_operands(T, K, N, E, seed=14)
+    ids = np.array([[0, 1], [2, 0], [1, 1], [2, 1], [0, 2], [1, 0]], dtype=np.int32)
+    w = np.linspace(0.1, 0.9, 12, dtype=np.float32).reshape(6, 2)
+    dy_deq = O.e4m3_decode(dyq) * sdy[:, None].astype(np.float64)
+    gdx, _, gdt = O.moe_backward(dy_deq, x, _w_deq(Wtq, swt), ids, w, bf16_operands=False)
+
+    def run(decode_w, scale_of, dot_scaled=True):
+        dx = np.zeros((T, K)); dt = np.zeros((T, 2))
+        for t in range(T):
+            for j in range(2):
+                e = ids[t, j]
+                G = (O.e4m3_decode(dyq[t]) @ decode_w(e).T) * scale_of(t, e)
+                dx[t] += w[t, j] * G
+                dt[t, j] = np.sum(x[t] * (G if dot_scaled else G / sdy[t]))
+        return dx, dt
+    right_w = lambda e: O.e4m3_decode(Wtq[e])                       # [K, N]
+    right_s = lambda t, e: sdy[t] * swt[e]
+    dx0, dt0 = run(right_w, right_s)
+    np.testing.assert_allclose(dx0, gdx, rtol=1e-12, atol=1e-13)    # the harness itself is right
+    bads = [
+        run(lambda e: O.e4m3_decode(Wtq[e]).T.reshape(K, N), right_s),   # codes not transposed
+        run(right_w, lambda t, e: sdy[t] * swt[e][::-1]),             # column scales reversed
+        run(right_w, lambda t, e: sdy[t] * swt[0]),                   # expert 0's scales for all
+        run(right_w, right_s, dot_scaled=False),                      # token scale left out of the dot
+    ]
+    for bdx, bdt in bads:
+        assert not (np.allclose(bdx, gdx, rtol=1e-9) and np.allclose(bdt, gdt, rtol=1e-9))
