@@ -490,6 +490,7 @@ def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush, peak_tf):
     res["bwd_split"] = _bwd_split_extra(dev, mgg, flush)
     res["dw_splitk"] = _dw_splitk_extra(dev, mgg, lib, flush)
     res["ffn_backward"] = _ffn_backward_extra(dev, mgg, lib, flush)
+    res["fp8_backward_dx"] = _fp8_backward_dx_extra(dev, mgg, lib, flush, peaks, peak_kind)
     fs, dec, be, bs = res["fwd_skew"], res["decode"], res["bare_e4"], res["bwd_split"]
     bwd_fl = 4.0 * 4096 * 2 * 2048 * 2048
     configs = {
@@ -507,6 +508,93 @@ def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush, peak_tf):
         "5_decode": {"ms": dec["ms"], "GB/s": dec["GB/s"], "frac": dec["roofline"]["frac"]},
     }
     return res, configs
+
+
+def _fp8_backward_dx_extra(dev, mgg, lib, flush, peaks, peak_kind):
+    """The e4m3 input gradient on the top-2 backward workload: dy quantised
+    per token, W per (expert, input column) and stored [E, K, N]; the timed
+    call is the schedule scan, the zeroing of dx and dtopk and the dX GEMM on
+    the codes.  The two quantisations are timed beside it (CUDA-graph
+    replays, L2 flushed before each)."""
+    import torch
+    import workloads
+    c = workloads.BWD_TOP2
+    p = workloads.moe_problem(**c)
+    T, K, N, E, k = c["T"], c["K"], c["N"], c["E"], c["k"]
+    x, W, dy = p["x"].to(dev), p["W"].to(dev), p["dy"].to(dev)
+    ids, w = p["expert_ids"].to(dev), p["topk_weights"].to(dev)
+    st = mgg.new_status(dev)
+    r = mgg.route(ids, w, E, N, status=st)
+    dyq, sdy = mgg.quantize_fp8(dy)
+    wtq, swt = mgg.quantize_fp8_cols(W)
+    dx = torch.empty(T, K, device=dev)
+    dt = torch.empty(T, k, device=dev)
+    ev, s0, s1 = Events(1), torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h = ev.handles()
+
+    def call():
+        mgg.moe_backward_dx_fp8(dyq, sdy, wtq, swt, x, r, k, status=st, dx=dx, dtopk=dt)
+    for _ in range(3):
+        call()
+    t_all, t_k = [], []
+    for _ in range(10):
+        flush.zero_()
+        lib.mgg_set_kernel_events(h, 1)
+        s0.record()
+        call()
+        s1.record()
+        lib.mgg_set_kernel_events(None, 0)
+        torch.cuda.synchronize()
+        t_all.append(s0.elapsed_time(s1))
+        t_k.append(ev.ms(0))
+
+    def replay_ms(fn, n=10):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                fn()
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        ts = []
+        for _ in range(n):
+            flush.zero_()
+            s0.record()
+            g.replay()
+            s1.record()
+            torch.cuda.synchronize()
+            ts.append(s0.elapsed_time(s1))
+        return statistics.mean(ts)
+    t_qdy = replay_ms(lambda: mgg.quantize_fp8(dy))
+    t_qw = replay_ms(lambda: mgg.quantize_fp8_cols(W))
+    if mgg.read_status(st) != 0:
+        raise RuntimeError("fp8 dX status set")
+    fl = 2.0 * T * k * K * N
+    gemm_tf = fl / (statistics.mean(t_k) * 1e-3) / 1e12
+    peak8 = 2.0 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    qw_bytes = E * N * K * 2 + E * N * K + E * K * 4
+    qdy_bytes = T * N * 4 + T * N + T * 4
+    out = {
+        "workload": "input and routing-weight gradients on e4m3 codes, dy per token, W per (expert, "
+                    "input column), top-2: T=4096, K=N=2048, E=8, k=2, uniform distinct routing; "
+                    "dy ~N(0,1); seed 0",
+        "ms": round(statistics.mean(t_all), 4), "gemm_ms": round(statistics.mean(t_k), 4),
+        "tflops": round(fl / (statistics.mean(t_all) * 1e-3) / 1e12, 1),
+        "gemm_tflops": round(gemm_tf, 1),
+        "quantize_dy_ms": round(t_qdy, 4),
+        "quantize_dy_GB/s": round(qdy_bytes / (t_qdy * 1e-3) / 1e9, 1),
+        "quantize_w_cols_ms": round(t_qw, 4),
+        "quantize_w_cols_GB/s": round(qw_bytes / (t_qw * 1e-3) / 1e9, 1),
+        "quantize_hbm_peak": hbm,
+        "roofline": {"bound": "tensor", "achieved": round(gemm_tf, 1), "peak": round(peak8, 1),
+                     "unit": "TFLOP/s", "frac": round(gemm_tf / peak8, 4),
+                     "peak_source": f"{peak_kind} bf16 dense (burst) x 2, the nominal e4m3/bf16 ratio",
+                     "traffic": None}}
+    del x, W, dy, dyq, wtq, dx, dt, r
+    return out
 
 
 def _ffn_backward_extra(dev, mgg, lib, flush):

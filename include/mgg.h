@@ -154,7 +154,8 @@ mgg_status mgg_tile_config(mgg_op op, mgg_dtype dtype, int* BM, int* BN, int* BK
  * Arguments that an op does not use are ignored (pass 0).  Returns 0 for an
  * invalid combination.
  *   MGG_OP_ROUTE, MGG_OP_FORWARD : T, k, E
- *   MGG_OP_BACKWARD              : T, k, E, N, K, dtype
+ *   MGG_OP_BACKWARD              : T, k, E, N, K, dtype (MGG_FP8_E4M3: the
+ *                                  e4m3 input gradient, mgg_moe_backward_dx_fp8)
  *   MGG_OP_GROUPED_GEMM          : E
  *   MGG_OP_MASKED                : 0 (no workspace)
  *   MGG_OP_FFN_FORWARD           : T, k, E (N = H, K = F unused)
@@ -363,6 +364,48 @@ mgg_status mgg_moe_forward_fp8(const uint8_t* x, const float* x_scale, const uin
                                const float* topk_weights, int T, int K, int N, int E, int k,
                                float* y, const mgg_routing* routing, int32_t* dev_status,
                                void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Per-column quantisation of the weights for the e4m3 input gradient, stored
+ * transposed: W [E, N, K] bf16 (16-byte aligned) ->
+ *   scale[e, k]   = max_n |W[e, n, k]| / 448   (IEEE f32 division; 1 for an
+ *                                              all-zero column)
+ *   Wtq[e, k, n]  = e4m3(W[e, n, k] / scale[e, k])  (as mgg_quantize_fp8)
+ * Wtq [E, K, N] uint8 and scale [E, K] f32, both 16-byte aligned.  The
+ * input gradient dx = dy W_e contracts over n, so a scale per (e, k) (and
+ * one per token for dy) factors out of the sum, as per-row scales do in the
+ * forward ("Grouped GEMM for MoE, in depth", §Choosing an implementation:
+ * FP8 scale factors that travel with each group).  N % 16 == 0 and
+ * K % 8 == 0 (MGG_ERR_ALIGNMENT); E <= 65535.  Errors: MGG_ERR_INVALID_ARG,
+ * MGG_ERR_ALIGNMENT, MGG_ERR_UNSUPPORTED_ARCH, MGG_ERR_CUDA.
+ */
+mgg_status mgg_quantize_fp8_cols(const void* W, int E, int N, int K, uint8_t* Wtq, float* scale,
+                                 void* stream);
+
+/*
+ * Input gradient and routing-weight gradient of the MoE layer on e4m3
+ * operands (the dx and dtopk of mgg_moe_backward; "Grouped GEMM for MoE, in
+ * depth", §The backward pass, input gradient; "grouped-gemm-moe", §How it
+ * works).  With e = expert_ids[t, j] and
+ *   G[t, j, k] = dy_scale[t] * wt_scale[e, k] * sum_n dyq[t, n] Wtq[e, k, n]
+ *   dx[t, k]    = sum_j topk_weights[t, j] * G[t, j, k]
+ *   dtopk[t, j] = sum_k x[t, k] * G[t, j, k]
+ * dyq [T, N] e4m3 codes with dy_scale [T] f32 (mgg_quantize_fp8 of dy),
+ * Wtq [E, K, N] with wt_scale [E, K] (mgg_quantize_fp8_cols of W), x [T, K]
+ * bf16; dx [T, K] and dtopk [T, k] f32, overwritten.  routing as filled by
+ * a forward of the same expert_ids/topk_weights (any N; the call tiles dx
+ * over K itself).  N % 16 == 0, K % 8 == 0; dyq, Wtq, x, dx and wt_scale
+ * 16-byte aligned (MGG_ERR_ALIGNMENT).  ws: mgg_workspace_bytes(
+ * MGG_OP_BACKWARD, T, k, E, N, K, MGG_FP8_E4M3).  Errors as for
+ * mgg_moe_backward.  The weight gradient has no e4m3 form: it contracts
+ * over the tokens of an expert, along which neither operand's scales are
+ * constant.
+ */
+mgg_status mgg_moe_backward_dx_fp8(const uint8_t* dyq, const float* dy_scale, const uint8_t* Wtq,
+                                   const float* wt_scale, const void* x,
+                                   const mgg_routing* routing, int T, int K, int N, int E, int k,
+                                   float* dx, float* dtopk, int32_t* dev_status, void* ws,
+                                   size_t ws_bytes, void* stream);
 
 /*
  * Gated expert FFN forward, one MoE layer ("Grouped GEMM for MoE, in depth",

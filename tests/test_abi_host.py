@@ -104,7 +104,25 @@ def test_fp8_invalid_arguments_rejected_before_launch(lib):
     assert (bm.value, bn.value, bk.value) == (256, 256, 128)   # 128 codes per stage row
     assert lib.mgg_tile_config(L.MGG_OP_BACKWARD, L.MGG_FP8_E4M3, ctypes.byref(bm),
                                ctypes.byref(bn), ctypes.byref(bk)) == L.MGG_ERR_DTYPE
-    assert lib.mgg_workspace_bytes(L.MGG_OP_BACKWARD, 64, 2, 8, 64, 64, L.MGG_FP8_E4M3) == 0
+    # the e4m3 backward is the input gradient only: two schedule arrays of E+1
+    assert lib.mgg_workspace_bytes(L.MGG_OP_BACKWARD, 64, 2, 8, 64, 64, L.MGG_FP8_E4M3) == 512
+    # column quantiser: null, N not a multiple of 16, K not a multiple of 8,
+    # misaligned scales
+    assert lib.mgg_quantize_fp8_cols(None, 2, 32, 16, fake, fake, None) == L.MGG_ERR_INVALID_ARG
+    assert lib.mgg_quantize_fp8_cols(fake, 2, 40, 16, fake, fake, None) == L.MGG_ERR_ALIGNMENT
+    assert lib.mgg_quantize_fp8_cols(fake, 2, 32, 20, fake, fake, None) == L.MGG_ERR_ALIGNMENT
+    assert lib.mgg_quantize_fp8_cols(fake, 2, 32, 16, fake, ctypes.c_void_p(0x10004),
+                                     None) == L.MGG_ERR_ALIGNMENT
+    # e4m3 input gradient: null x, N % 16, K % 8, misaligned column scales,
+    # short workspace
+    def dxf8(x=fake, N=32, K=16, wts=fake, nbytes=1 << 20):
+        return lib.mgg_moe_backward_dx_fp8(fake, fake, fake, wts, x, ctypes.byref(r), 4, K, N, 2,
+                                           1, fake, fake, fake, fake, nbytes, None)
+    assert dxf8(x=None) == L.MGG_ERR_INVALID_ARG
+    assert dxf8(N=40) == L.MGG_ERR_ALIGNMENT
+    assert dxf8(K=12) == L.MGG_ERR_ALIGNMENT
+    assert dxf8(wts=ctypes.c_void_p(0x10004)) == L.MGG_ERR_ALIGNMENT
+    assert dxf8(nbytes=16) == L.MGG_ERR_WORKSPACE
     # quantisation: null, columns not a multiple of 16, source dtype
     assert lib.mgg_quantize_fp8(None, L.MGG_BF16, 4, 16, fake, fake, None) == L.MGG_ERR_INVALID_ARG
     assert lib.mgg_quantize_fp8(fake, L.MGG_BF16, 4, 24, fake, fake, None) == L.MGG_ERR_ALIGNMENT

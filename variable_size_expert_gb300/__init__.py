@@ -10,5 +10,6 @@ from .ops import (  # noqa: F401
     moe_ffn_backward, moe_ffn_forward, moe_forward, new_status, read_status, route, tile_config,
     workspace_bytes,
     quantize_fp8, moe_forward_fp8, grouped_gemm_fp8, grouped_gemm_masked_fp8,
+    quantize_fp8_cols, moe_backward_dx_fp8,
 )
 from . import _lib  # noqa: F401

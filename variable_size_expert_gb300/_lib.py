@@ -48,7 +48,8 @@ EXPORTS = (
     "mgg_grouped_gemm", "mgg_moe_forward", "mgg_moe_backward", "mgg_debug_tile_schedule",
     "mgg_set_kernel_events", "mgg_route_noalloc", "mgg_moe_ffn_forward", "mgg_quantize_fp8",
     "mgg_grouped_gemm_fp8", "mgg_moe_forward_fp8", "mgg_moe_ffn_backward",
-    "mgg_debug_wait_timeout", "mgg_debug_row_tile",
+    "mgg_debug_wait_timeout", "mgg_debug_row_tile", "mgg_quantize_fp8_cols",
+    "mgg_moe_backward_dx_fp8",
 )
 
 
@@ -88,6 +89,9 @@ _SIGS = {
     "mgg_moe_ffn_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _RP, _I, _I, _I, _I, _I, _I, _P, _P,
                                   _P, _P, _P, _P, _P, _SZ, _P]),
     "mgg_quantize_fp8": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "mgg_quantize_fp8_cols": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "mgg_moe_backward_dx_fp8": (_I, [_P, _P, _P, _P, _P, _RP, _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                                     _SZ, _P]),
     "mgg_grouped_gemm_fp8": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "mgg_moe_forward_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _RP, _P, _P, _SZ,
                                  _P]),

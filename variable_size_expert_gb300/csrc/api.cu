@@ -424,6 +424,7 @@ size_t mgg_workspace_bytes(mgg_op op, int T, int k, int E, int N, int K, mgg_dty
       return route_ws_bytes(T, k, E);
     case MGG_OP_BACKWARD:
       if (T < 1 || k < 1 || E < 1 || E > kMaxExperts || N < 1 || K < 1) return 0;
+      if (dtype == MGG_FP8_E4M3) return 2 * round256((E + 1) * sizeof(int32_t));  // dX only
       if (dtype != MGG_BF16 && dtype != MGG_F32) return 0;
       return bwd_layout(T, k, E, N, K, dtype).total;
     case MGG_OP_GROUPED_GEMM:
@@ -752,6 +753,73 @@ mgg_status mgg_quantize_fp8(const void* src, mgg_dtype src_dtype, int rows, int 
   if (s != MGG_OK) return s;
   return from_cuda(launch_quantize_fp8(src, src_dtype == MGG_F32, rows, cols, q, scale,
                                        static_cast<cudaStream_t>(stream)));
+}
+
+mgg_status mgg_quantize_fp8_cols(const void* W, int E, int N, int K, uint8_t* Wtq, float* scale,
+                                 void* stream) {
+  if (!W || !Wtq || !scale) return MGG_ERR_INVALID_ARG;
+  if (E < 1 || N < 1 || K < 1 || E > 65535) return MGG_ERR_INVALID_ARG;
+  if (N % 16 != 0 || K % 8 != 0 || !aligned(W, 16) || !aligned(Wtq, 16) || !aligned(scale, 16))
+    return MGG_ERR_ALIGNMENT;
+  mgg_status s = check_arch();
+  if (s != MGG_OK) return s;
+  return from_cuda(
+      launch_quantize_fp8_cols(W, E, N, K, Wtq, scale, static_cast<cudaStream_t>(stream)));
+}
+
+mgg_status mgg_moe_backward_dx_fp8(const uint8_t* dyq, const float* dy_scale, const uint8_t* Wtq,
+                                   const float* wt_scale, const void* x,
+                                   const mgg_routing* routing, int T, int K, int N, int E, int k,
+                                   float* dx, float* dtopk, int32_t* dev_status, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  if (!dyq || !dy_scale || !Wtq || !wt_scale || !x || !routing_ok(routing) || !dx || !dtopk ||
+      !dev_status || !ws)
+    return MGG_ERR_INVALID_ARG;
+  if (T < 1 || K < 1 || N < 1 || E < 1 || k < 1 || E > kMaxExperts) return MGG_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * k > (1LL << 30)) return MGG_ERR_INVALID_ARG;
+  if (N % 16 != 0 || K % 8 != 0) return MGG_ERR_ALIGNMENT;
+  if (!aligned(dyq, 16) || !aligned(Wtq, 16) || !aligned(x, 16) || !aligned(dx, 16) ||
+      !aligned(wt_scale, 16) || !aligned(dy_scale, 4) || !aligned(dtopk, 4))
+    return MGG_ERR_ALIGNMENT;
+  if (ws_bytes < mgg_workspace_bytes(MGG_OP_BACKWARD, T, k, E, N, K, MGG_FP8_E4M3) ||
+      !aligned(ws, 256))
+    return MGG_ERR_WORKSPACE;
+  mgg_status s = check_arch();
+  if (s != MGG_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* tile_start_dx = at<int32_t>(ws, 0);
+  int32_t* pstart = at<int32_t>(ws, round256((E + 1) * sizeof(int32_t)));
+  // dX tiles over the K output columns; dx and dtopk take atomic adds
+  if (launch_bwd_scan(routing->counts, E, kPairBM, cdiv(K, kPairBN), kDwPad, tile_start_dx, pstart,
+                      st) != cudaSuccess ||
+      cudaMemsetAsync(dx, 0, static_cast<size_t>(T) * K * sizeof(float), st) != cudaSuccess ||
+      cudaMemsetAsync(dtopk, 0, static_cast<size_t>(T) * k * sizeof(float), st) != cudaSuccess)
+    return MGG_ERR_CUDA;
+  const int Nu = N / 2;  // e4m3 rows move as 16-bit units
+  RowsParams p{};
+  p.A = dyq;
+  p.lda = Nu;
+  p.Kc = Nu;
+  p.row_token = routing->row_token;
+  p.row_weight = routing->row_weight;
+  p.row_assign = routing->row_assign;
+  p.tile_start = tile_start_dx;
+  p.start = routing->start;
+  p.E = E;
+  p.Nout = K;
+  p.out = dx;
+  p.ldo = K;
+  p.xdot = x;
+  p.ldx = K;
+  p.dtopk = dtopk;
+  p.a_scale = dy_scale;
+  p.b_scale = wt_scale;
+  p.dev_status = dev_status;
+  p.wait_limit = wait_limit();
+  CUtensorMap tm;  // Wtq [E, K, N]: K-major rows of N codes
+  if (!tmap_weights(&tm, Wtq, E, K, Nu, kBK, kPairBN / 2)) return MGG_ERR_CUDA;
+  return from_cuda(
+      timed(0, st, [&] { return launch_rows_pair(kModeFusedDtopk, false, tm, tm, p, st, true); }));
 }
 
 mgg_status mgg_grouped_gemm_fp8(const uint8_t* A, const float* a_scale, const uint8_t* W,

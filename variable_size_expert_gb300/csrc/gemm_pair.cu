@@ -252,10 +252,14 @@ __device__ __forceinline__ float sigmoid_fast(float v) {
 }
 
 // ====================================================================== rows
-// F8: e4m3 operands (fused and bare modes, both K-major).  A stage still
+// F8: e4m3 operands (fused, bare and dX modes, all K-major).  A stage still
 // holds 128-byte rows, now of 128 codes, moved by the same gather and TMA
 // code as 16-bit units; the MMA is kind::f8f6f4 (K = 32 per instruction) and
-// the epilogue applies the row and column scales.
+// the epilogue applies the row and column scales.  In the dX mode A is dy
+// quantised per token and B the weights quantised per (expert, input
+// column), stored [E, K, N], so both scales factor out of the sum over n;
+// the routing-weight dot takes the column-scaled values and its sum is
+// multiplied by the token's scale.
 template <int MODE, bool B_MN, bool F8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 1)
     rows_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -272,8 +276,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
   constexpr bool GATHER =
       MODE == kModeFused || MODE == kModeFusedDtopk || GATEUP || SWIGLU;
   constexpr bool SCATTER = MODE == kModeFused || MODE == kModeFusedDtopk || MODE == kModeScatter;
-  static_assert(!F8 || ((MODE == kModeFused || MODE == kModeBare) && !B_MN),
-                "e4m3 operands: fused and bare modes, K-major");
+  static_assert(!F8 || ((MODE == kModeFused || MODE == kModeBare || MODE == kModeFusedDtopk) &&
+                        !B_MN),
+                "e4m3 operands: fused, bare and dX modes, K-major");
   constexpr int EPW = rows_epi_warps(MODE);  // epilogue warps
   constexpr int CW = rows_epi_cols(MODE);    // columns per staged block
   constexpr int LPR = CW / 4;                // lanes per staged row after the transpose
@@ -797,7 +802,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(rows_threads(MODE), 
 #pragma unroll
           for (int o = 1; o < LPR; o <<= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
           const int r = ro + rq + RSTEP * j;
-          if (kq == 0 && r < t.rows) atomicAdd(p.dtopk + __ldg(p.row_assign + t.row0 + r), d);
+          if (kq == 0 && r < t.rows) {
+            if (F8) d *= __ldg(p.a_scale + orow[j]);  // the token's dy scale
+            atomicAdd(p.dtopk + __ldg(p.row_assign + t.row0 + r), d);
+          }
         }
       }
       ++tcount;
@@ -1331,6 +1339,8 @@ cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_
     if (mode == kModeBare) return launch_rows_pair_t<kModeBare, false, true>(tmap_a, tmap_b, p, st);
     if (mode == kModeFused)
       return launch_rows_pair_t<kModeFused, false, true>(tmap_a, tmap_b, p, st);
+    if (mode == kModeFusedDtopk)
+      return launch_rows_pair_t<kModeFusedDtopk, false, true>(tmap_a, tmap_b, p, st);
     return cudaErrorInvalidValue;
   }
   if (!b_mn_major) {

@@ -189,7 +189,7 @@ cudaError_t launch_debug_schedule(const int32_t* tile_start, const int32_t* star
                                   int max_tiles, int32_t* out, cudaStream_t st);
 
 // gemm_pair.cu (tcgen05, cta_group::2)
-// f8: e4m3 operands (kModeFused and kModeBare, both K-major)
+// f8: e4m3 operands (kModeFused, kModeBare and kModeFusedDtopk, all K-major)
 cudaError_t launch_rows_pair(int mode, bool b_mn_major, const CUtensorMap& tmap_a,
                              const CUtensorMap& tmap_b, const RowsParams& p, cudaStream_t st,
                              bool f8 = false);
@@ -209,6 +209,9 @@ cudaError_t launch_masked_gemm(const CUtensorMap& tmap_w, const MaskedParams& p,
 // quant.cu: per-row e4m3 quantisation of a [rows, cols] bf16 or f32 matrix
 cudaError_t launch_quantize_fp8(const void* src, bool src_f32, int rows, int cols, uint8_t* q,
                                 float* scale, cudaStream_t st);
+// W [E, N, K] bf16 -> codes [E, K, N] and scale [E, K], per (expert, column k)
+cudaError_t launch_quantize_fp8_cols(const void* W, int E, int N, int K, uint8_t* q, float* scale,
+                                     cudaStream_t st);
 
 // simt_f32.cu (exact f32 path)
 cudaError_t launch_rows_f32(int mode, bool w_transposed, const RowsParams& p, const float* W,

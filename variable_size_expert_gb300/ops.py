@@ -10,7 +10,8 @@ Functions mirror the pages' usage ("grouped-gemm-moe", §Usage):
 plus the lower-level calls (route, moe_forward, moe_backward,
 grouped_gemm_masked, debug_tile_schedule) and the e4m3 forms with per-row
 scales (quantize_fp8, moe_forward_fp8, grouped_gemm_fp8,
-grouped_gemm_masked_fp8).
+grouped_gemm_masked_fp8) and per-column weight scales for the input
+gradient (quantize_fp8_cols, moe_backward_dx_fp8).
 """
 from __future__ import annotations
 
@@ -25,7 +26,7 @@ __all__ = [
     "RoutingBuffers", "route", "moe_forward", "moe_backward", "moe", "grouped_gemm",
     "grouped_gemm_masked", "debug_tile_schedule", "tile_config", "workspace_bytes",
     "moe_ffn_forward", "quantize_fp8", "moe_forward_fp8", "grouped_gemm_fp8",
-    "grouped_gemm_masked_fp8",
+    "grouped_gemm_masked_fp8", "quantize_fp8_cols", "moe_backward_dx_fp8",
     "new_status", "read_status",
 ]
 
@@ -378,6 +379,55 @@ def moe_forward_fp8(xq: torch.Tensor, x_scale: torch.Tensor, Wq: torch.Tensor,
                                     _ptr(y), ctypes.byref(rs), _ptr(st), _ptr(ws), ws.numel(),
                                     _stream()), "mgg_moe_forward_fp8")
     return y, r
+
+
+def quantize_fp8_cols(W: torch.Tensor):
+    """Per-(expert, input column) e4m3 quantisation of W [E, N, K] (bfloat16),
+    stored transposed: returns (codes uint8 [E, K, N], scale float32 [E, K])
+    with W[e, n, k] ~ decode(codes[e, k, n]) * scale[e, k]
+    (mgg_quantize_fp8_cols)."""
+    lib = L.load()
+    if W.dtype != torch.bfloat16 or W.dim() != 3:
+        raise TypeError("W must be a bfloat16 [E, N, K] tensor")
+    W = W.contiguous()
+    E, N, K = W.shape
+    q = torch.empty(E, K, N, dtype=torch.uint8, device=W.device)
+    scale = torch.empty(E, K, dtype=torch.float32, device=W.device)
+    L.check(lib.mgg_quantize_fp8_cols(_ptr(W), E, N, K, _ptr(q), _ptr(scale), _stream()),
+            "mgg_quantize_fp8_cols")
+    return q, scale
+
+
+def moe_backward_dx_fp8(dyq: torch.Tensor, dy_scale: torch.Tensor, Wtq: torch.Tensor,
+                        wt_scale: torch.Tensor, x: torch.Tensor, routing: RoutingBuffers, k: int,
+                        status: torch.Tensor | None = None, dx=None, dtopk=None,
+                        workspace: torch.Tensor | None = None):
+    """Input and routing-weight gradients on e4m3 operands: dy quantised per
+    token (dyq [T, N], dy_scale [T]) and W per input column (Wtq [E, K, N],
+    wt_scale [E, K], from quantize_fp8_cols); x [T, K] bfloat16.  Returns
+    (dx [T, K], dtopk [T, k]), float32 (mgg_moe_backward_dx_fp8)."""
+    lib = L.load()
+    dyq, Wtq = _codes(dyq), _codes(Wtq)
+    T, N = dyq.shape
+    E, K, N2 = Wtq.shape
+    if N2 != N or tuple(x.shape) != (T, K):
+        raise ValueError("dyq [T, N], Wtq [E, K, N] and x [T, K] must agree")
+    if x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16")
+    dev = dyq.device
+    x = x.contiguous()
+    dx = dx if dx is not None else torch.empty(T, K, dtype=torch.float32, device=dev)
+    dtopk = dtopk if dtopk is not None else torch.empty(T, k, dtype=torch.float32, device=dev)
+    st = status if status is not None else new_status(dev)
+    nbytes = lib.mgg_workspace_bytes(L.MGG_OP_BACKWARD, T, k, E, N, K, L.MGG_FP8_E4M3)
+    ws = workspace if workspace is not None and workspace.numel() >= nbytes else _workspace(nbytes, dev)
+    rs = routing.struct()
+    L.check(lib.mgg_moe_backward_dx_fp8(_ptr(dyq.contiguous()), _ptr(dy_scale.contiguous()),
+                                        _ptr(Wtq.contiguous()), _ptr(wt_scale.contiguous()), _ptr(x),
+                                        ctypes.byref(rs), T, K, N, E, k, _ptr(dx), _ptr(dtopk),
+                                        _ptr(st), _ptr(ws), ws.numel(), _stream()),
+            "mgg_moe_backward_dx_fp8")
+    return dx, dtopk
 
 
 def grouped_gemm_fp8(aq: torch.Tensor, a_scale: torch.Tensor, Wq: torch.Tensor,
