@@ -298,17 +298,19 @@ __global__ void __launch_bounds__(1024)
       hist[b * E + e] = m;
     }
   }
-  grid.sync();  // every block's totals are published
   if (!router) {
-    // the other blocks zero y after the barrier, so the routing blocks'
-    // second pass runs beside the zeroing instead of after it (only the
-    // kernel's completion orders y before the GEMM's atomic adds)
+    // The other blocks only arrive at the grid barrier (the routing blocks
+    // read nothing of theirs) and zero y at once, beside both routing
+    // passes; only the kernel's completion orders y before the GEMM's
+    // atomic adds.
+    (void)grid.barrier_arrive();
     const long long stride = static_cast<long long>(gridDim.x - nb) * blockDim.x;
     for (long long i = static_cast<long long>(b - nb) * blockDim.x + threadIdx.x; i < nzero4;
          i += stride)
       zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
+  grid.sync();  // every routing block's totals are published
   const int e = threadIdx.x;
   int m = 0, before = 0;
   if (e < E)
@@ -588,31 +590,48 @@ __global__ void __launch_bounds__(kPrepThreads)
           wj = __ldg(row_weight + r);
         }
       }
-      // uniform trip count: the shuffles below need the whole warp
-#pragma unroll 2
-      for (int i0 = 0; i0 < n8; i0 += 32) {
-        const int i = i0 + lane;
-        const bool act = i < n8;
-        const float4 a = act ? __ldg(src + 2 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 b = act ? __ldg(src + 2 * i + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j0 == 0 && act) {
-          uint4 q;
-          q.x = pack_bf16x2(a.x, a.y);
-          q.y = pack_bf16x2(a.z, a.w);
-          q.z = pack_bf16x2(b.x, b.y);
-          q.w = pack_bf16x2(b.z, b.w);
-          outb[i] = q;
+      // uniform trip count: the shuffles below need the whole warp.  A
+      // chunk is 8 x 32 pieces of 8 values (a row of up to 2048), all of
+      // its loads issued before the first use
+      constexpr int CH = 8;
+      for (int i0 = 0; i0 < n8; i0 += 32 * CH) {
+        float4 a[CH], b[CH];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int i = i0 + 32 * c + lane;
+          const bool act = i < n8;
+          a[c] = act ? __ldg(src + 2 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          b[c] = act ? __ldg(src + 2 * i + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (j0 == 0) {
+#pragma unroll
+          for (int c = 0; c < CH; ++c) {
+            const int i = i0 + 32 * c + lane;
+            if (i < n8) {
+              uint4 q;
+              q.x = pack_bf16x2(a[c].x, a[c].y);
+              q.y = pack_bf16x2(a[c].z, a[c].w);
+              q.z = pack_bf16x2(b[c].x, b[c].y);
+              q.w = pack_bf16x2(b[c].z, b[c].w);
+              outb[i] = q;
+            }
+          }
         }
         for (int j = 0; j < nj; ++j) {
           const int p = __shfl_sync(0xffffffffu, pj, j);
           const float wr = __shfl_sync(0xffffffffu, wj, j);
-          if (p >= 0 && act) {
-            uint4 o;
-            o.x = pack_bf16x2(__fmul_rn(wr, a.x), __fmul_rn(wr, a.y));
-            o.y = pack_bf16x2(__fmul_rn(wr, a.z), __fmul_rn(wr, a.w));
-            o.z = pack_bf16x2(__fmul_rn(wr, b.x), __fmul_rn(wr, b.y));
-            o.w = pack_bf16x2(__fmul_rn(wr, b.z), __fmul_rn(wr, b.w));
-            dyw[static_cast<size_t>(p) * n8 + i] = o;
+          if (p < 0) continue;
+#pragma unroll
+          for (int c = 0; c < CH; ++c) {
+            const int i = i0 + 32 * c + lane;
+            if (i < n8) {
+              uint4 o;
+              o.x = pack_bf16x2(__fmul_rn(wr, a[c].x), __fmul_rn(wr, a[c].y));
+              o.y = pack_bf16x2(__fmul_rn(wr, a[c].z), __fmul_rn(wr, a[c].w));
+              o.z = pack_bf16x2(__fmul_rn(wr, b[c].x), __fmul_rn(wr, b[c].y));
+              o.w = pack_bf16x2(__fmul_rn(wr, b[c].z), __fmul_rn(wr, b[c].w));
+              dyw[static_cast<size_t>(p) * n8 + i] = o;
+            }
           }
         }
       }
@@ -752,7 +771,18 @@ cudaError_t launch_bwd_prep(const float* dy, int T, int N, int K, int k, const i
                             const DwSplitPlan* split) {
   const int wpb = kPrepThreads / 32;
   const int items = std::max(T, S_pad_max);
-  const int blocks = std::max(1, std::min(cdiv(items, wpb), num_sms() * (2048 / kPrepThreads)));
+  // one wave of resident blocks (each walks tokens with a grid stride): the
+  // per-block prologue (the schedule scans) is paid once per SM slot
+  static int resident = 0;
+  if (resident == 0) {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, bwd_prep_kernel, kPrepThreads, 0) !=
+            cudaSuccess ||
+        nb < 1)
+      nb = 1;
+    resident = nb;
+  }
+  const int blocks = std::max(1, std::min(cdiv(items, wpb), num_sms() * resident));
   int32_t* order = expert_order && E <= kPrepThreads ? expert_order : nullptr;
   // the split plan is published in visiting order, so it needs the order
   DwSplitPlan sp{};
