@@ -43,8 +43,9 @@ def _quant_rows_both(src: torch.Tensor):
     return rq, rs
 
 
+# columns from 16 to 9216 rows long, K ragged against the 32-column slab
 @pytest.mark.parametrize("E,N,K", [(1, 16, 8), (3, 48, 72), (2, 2048, 136), (8, 96, 2048),
-                                   (5, 1040, 264)])
+                                   (5, 1040, 264), (1, 8192, 40), (1, 8208, 8), (2, 9216, 72)])
 def test_quantize_cols_bit_exact(E, N, K):
     rng = np.random.default_rng(E * 1000 + N + K)
     W = rng.standard_normal((E, N, K)).astype(np.float32)
