@@ -330,7 +330,11 @@ def run_ours(args, ws, rank, local):
         "tflops": round(gemm_flops / (statistics.mean(t_fcall) * 1e-3) / 1e12, 1),
         "gemm_ms": round(kern["fwd_gather_scatter_gemm"], 4),
         "gemm_frac": round(gemm_flops / (kern["fwd_gather_scatter_gemm"] * 1e-3) / 1e12 / peak_tf, 4)}}
-    if rank == 0 and not args.no_extras:
+    if rank == 0 and args.only_extra == "fp8_backward_dx":
+        # one extra alone (a short command for profiling its kernels)
+        out["extras"] = {"fp8_backward_dx": _fp8_backward_dx_extra(dev, mgg, lib, flush, peaks,
+                                                                   peak_kind)}
+    elif rank == 0 and not args.no_extras:
         out["extras"], more = run_extras(dev, mgg, L, lib, peaks, peak_kind, flush, peak_tf)
         configs.update(more)
         configs["4_bwd_top2"].update(
@@ -1150,6 +1154,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--only-extra", choices=["fp8_backward_dx"], default=None,
+                    help="run this extra alone instead of all of them")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-csv", default=None,
                     help="also keep the raw nvidia-smi clock samples of the timed region here")
