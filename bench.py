@@ -596,7 +596,7 @@ def _fp8_backward_dx_extra(dev, mgg, lib, flush, peaks, peak_kind):
         "roofline": {"bound": "tensor", "achieved": round(gemm_tf, 1), "peak": round(peak8, 1),
                      "unit": "TFLOP/s", "frac": round(gemm_tf / peak8, 4),
                      "peak_source": f"{peak_kind} bf16 dense (burst) x 2, the nominal e4m3/bf16 ratio",
-                     "traffic": None}}
+                     "traffic": load_traffic("fp8_dx_dtopk_gemm")}}
     del x, W, dy, dyq, wtq, dx, dt, r
     return out
 
