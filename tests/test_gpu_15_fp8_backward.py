@@ -82,6 +82,7 @@ def _run(p, dyq, sdy, wtq, swt):
     (513, 136, 2064, 5, 3, "random", 3),
     (40, 128, 512, 200, 2, "random", 4),
     (130, 72, 96, 2, 3, "random", 5),
+    (700, 64, 32, 1024, 4, "random", 6),   # most of 1024 experts empty; chunked router
 ])
 def test_moe_backward_dx_fp8_vs_oracle(T, K, N, E, k, routing, seed):
     p = workloads.moe_problem(T=T, K=K, N=N, E=E, k=k, seed=seed, routing=routing, with_dy=True)
@@ -107,6 +108,45 @@ def test_fp8_dx_close_to_bf16_dx():
     torch.cuda.synchronize()
     assert O.rel_frobenius(f64(dx8), f64(dx)) < 0.06
     assert O.rel_frobenius(f64(dt8), f64(dt)) < 0.06
+
+
+def test_fp8_backward_graph_replay():
+    """The dy quantisation and the e4m3 dX call captured once in a CUDA graph
+    and replayed on new dy give the eager calls' bits (k = 2: each dx
+    element receives two adds onto zero; dtopk sums the partial dots of
+    several column blocks, so it is compared to float32 rounding)."""
+    T, K, N, E, k = 512, 512, 384, 8, 2
+    p = workloads.moe_problem(T=T, K=K, N=N, E=E, k=k, seed=21, with_dy=True)
+    x, W = p["x"].to(DEV), p["W"].to(DEV)
+    ids, w = p["expert_ids"].to(DEV), p["topk_weights"].to(DEV)
+    st = mgg.new_status(DEV)
+    r = mgg.route(ids, w, E, N, status=st)
+    wtq, swt = mgg.quantize_fp8_cols(W)
+    dy = p["dy"].to(DEV).clone()
+    dx = torch.empty(T, K, device=DEV)
+    dt = torch.empty(T, k, device=DEV)
+
+    def step():
+        dyq, sdy = mgg.quantize_fp8(dy)
+        mgg.moe_backward_dx_fp8(dyq, sdy, wtq, swt, x, r, k, status=st, dx=dx, dtopk=dt)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for seed in (1, 2):
+        dy.copy_(torch.randn(T, N, generator=torch.Generator().manual_seed(seed)).to(DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        gx, gt = dx.clone(), dt.clone()
+        step()
+        torch.cuda.synchronize()
+        assert torch.equal(gx, dx)
+        assert torch.allclose(gt, dt, rtol=1e-5, atol=1e-5)
+    assert mgg.read_status(st) == 0
 
 
 @pytest.mark.slow
