@@ -22,6 +22,9 @@
  *   CUDA graph.  (The bf16 backward forks onto a side stream, one per host
  *   thread and device, created with its two events on first use, and joins
  *   back; see mgg_moe_backward.)
+ * - Each entry point that enqueues work opens an NVTX range named after
+ *   itself for the duration of the host call (profiler timelines group the
+ *   call's kernels under it; no cost without a tool attached).
  * - Layouts are dense row-major with the shapes given; no strides.
  * - "bf16" tensors hold IEEE bfloat16 bit patterns (uint16); "f32" tensors
  *   hold binary32.  Outputs are always f32 and are fully overwritten by the

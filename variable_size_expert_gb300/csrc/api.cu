@@ -446,6 +446,7 @@ size_t mgg_workspace_bytes(mgg_op op, int T, int k, int E, int N, int K, mgg_dty
 mgg_status mgg_route(const int32_t* expert_ids, const float* topk_weights, int T, int k, int E,
                      int N, mgg_dtype dtype, const mgg_routing* routing, int32_t* dev_status,
                      void* ws, size_t ws_bytes, void* stream) {
+  const NvtxRange nvtx("mgg_route");
   if (!expert_ids || !topk_weights || !routing_ok(routing) || !dev_status || !ws)
     return MGG_ERR_INVALID_ARG;
   if (T < 1 || k < 1 || E < 1 || N < 1 || E > kMaxExperts) return MGG_ERR_INVALID_ARG;
@@ -467,6 +468,7 @@ mgg_status mgg_grouped_gemm(const void* A, const void* W, float* C, mgg_dtype dt
                             mgg_layout layout, const int32_t* offs, int rows_or_Mmax, int E,
                             int N, int K, int32_t* dev_status, void* ws, size_t ws_bytes,
                             void* stream) {
+  const NvtxRange nvtx("mgg_grouped_gemm");
   if (!A || !W || !C || !offs || !dev_status) return MGG_ERR_INVALID_ARG;
   if (rows_or_Mmax < 1 || E < 1 || N < 1 || K < 1 || E > kMaxExperts) return MGG_ERR_INVALID_ARG;
   if (dtype != MGG_BF16 && dtype != MGG_F32) return MGG_ERR_DTYPE;
@@ -537,6 +539,7 @@ mgg_status mgg_moe_forward(const void* x, const void* W, const int32_t* expert_i
                            const float* topk_weights, int T, int K, int N, int E, int k,
                            mgg_dtype dtype, float* y, const mgg_routing* routing,
                            int32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  const NvtxRange nvtx("mgg_moe_forward");
   if (!x || !W || !expert_ids || !topk_weights || !y || !routing_ok(routing) || !dev_status || !ws)
     return MGG_ERR_INVALID_ARG;
   mgg_status s = check_moe_sizes(T, K, N, E, k, dtype);
@@ -586,6 +589,7 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
                             const mgg_routing* routing, int T, int K, int N, int E, int k,
                             mgg_dtype dtype, float* dx, float* dW, float* dtopk,
                             int32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  const NvtxRange nvtx("mgg_moe_backward");
   if (!dy || !x || !W || !routing_ok(routing) || !dx || !dW || !dtopk || !dev_status || !ws)
     return MGG_ERR_INVALID_ARG;
   mgg_status s = check_moe_sizes(T, K, N, E, k, dtype);
@@ -744,6 +748,7 @@ mgg_status mgg_moe_backward(const float* dy, const void* x, const void* W,
 
 mgg_status mgg_quantize_fp8(const void* src, mgg_dtype src_dtype, int rows, int cols,
                             uint8_t* q, float* scale, void* stream) {
+  const NvtxRange nvtx("mgg_quantize_fp8");
   if (!src || !q || !scale) return MGG_ERR_INVALID_ARG;
   if (rows < 1 || cols < 1) return MGG_ERR_INVALID_ARG;
   if (src_dtype != MGG_BF16 && src_dtype != MGG_F32) return MGG_ERR_DTYPE;
@@ -757,6 +762,7 @@ mgg_status mgg_quantize_fp8(const void* src, mgg_dtype src_dtype, int rows, int 
 
 mgg_status mgg_quantize_fp8_cols(const void* W, int E, int N, int K, uint8_t* Wtq, float* scale,
                                  void* stream) {
+  const NvtxRange nvtx("mgg_quantize_fp8_cols");
   if (!W || !Wtq || !scale) return MGG_ERR_INVALID_ARG;
   if (E < 1 || N < 1 || K < 1 || E > 65535) return MGG_ERR_INVALID_ARG;
   if (N % 16 != 0 || K % 8 != 0 || !aligned(W, 16) || !aligned(Wtq, 16) || !aligned(scale, 16))
@@ -772,6 +778,7 @@ mgg_status mgg_moe_backward_dx_fp8(const uint8_t* dyq, const float* dy_scale, co
                                    const mgg_routing* routing, int T, int K, int N, int E, int k,
                                    float* dx, float* dtopk, int32_t* dev_status, void* ws,
                                    size_t ws_bytes, void* stream) {
+  const NvtxRange nvtx("mgg_moe_backward_dx_fp8");
   if (!dyq || !dy_scale || !Wtq || !wt_scale || !x || !routing_ok(routing) || !dx || !dtopk ||
       !dev_status || !ws)
     return MGG_ERR_INVALID_ARG;
@@ -826,6 +833,7 @@ mgg_status mgg_grouped_gemm_fp8(const uint8_t* A, const float* a_scale, const ui
                                 const float* w_scale, float* C, mgg_layout layout,
                                 const int32_t* offs, int rows_or_Mmax, int E, int N, int K,
                                 int32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  const NvtxRange nvtx("mgg_grouped_gemm_fp8");
   if (!A || !a_scale || !W || !w_scale || !C || !offs || !dev_status) return MGG_ERR_INVALID_ARG;
   if (rows_or_Mmax < 1 || E < 1 || N < 1 || K < 1 || E > kMaxExperts) return MGG_ERR_INVALID_ARG;
   if (layout != MGG_LAYOUT_CONTIGUOUS && layout != MGG_LAYOUT_MASKED &&
@@ -894,6 +902,7 @@ mgg_status mgg_moe_forward_fp8(const uint8_t* x, const float* x_scale, const uin
                                const float* topk_weights, int T, int K, int N, int E, int k,
                                float* y, const mgg_routing* routing, int32_t* dev_status,
                                void* ws, size_t ws_bytes, void* stream) {
+  const NvtxRange nvtx("mgg_moe_forward_fp8");
   if (!x || !x_scale || !W || !w_scale || !expert_ids || !topk_weights || !y ||
       !routing_ok(routing) || !dev_status || !ws)
     return MGG_ERR_INVALID_ARG;
@@ -941,6 +950,7 @@ mgg_status mgg_moe_ffn_forward(const void* x, const void* Wg, const void* Wu, co
                                int H, int F, int E, int k, mgg_dtype dtype, float* y, void* h,
                                float* gu, const mgg_routing* routing, int32_t* dev_status,
                                void* ws, size_t ws_bytes, void* stream) {
+  const NvtxRange nvtx("mgg_moe_ffn_forward");
   if (!x || !Wg || !Wu || !Wd || !expert_ids || !topk_weights || !y || !h ||
       !routing_ok(routing) || !dev_status || !ws)
     return MGG_ERR_INVALID_ARG;
@@ -1021,6 +1031,7 @@ mgg_status mgg_moe_ffn_backward(const float* dy, const void* x, const void* Wg, 
                                 mgg_dtype dtype, float* dx, float* dWg, float* dWu, float* dWd,
                                 float* dtopk, int32_t* dev_status, void* ws, size_t ws_bytes,
                                 void* stream) {
+  const NvtxRange nvtx("mgg_moe_ffn_backward");
   if (!dy || !x || !Wg || !Wu || !Wd || !h || !gu || !routing_ok(routing) || !dx || !dWg ||
       !dWu || !dWd || !dtopk || !dev_status || !ws)
     return MGG_ERR_INVALID_ARG;

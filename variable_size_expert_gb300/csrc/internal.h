@@ -7,7 +7,18 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace mgg {
+
+// An NVTX range over one C-ABI call, named after the entry point, so that
+// profiler timelines group each call's kernels (no cost without a tool).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Tile shapes of the tensor-core kernels.
 constexpr int kPairBM = 256;   // CTA-pair tile rows (MMA M, 128 per CTA)

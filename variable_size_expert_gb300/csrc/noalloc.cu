@@ -50,6 +50,7 @@ extern "C" mgg_status mgg_route_noalloc(const int32_t* expert_ids, const float* 
                                         int T, int k, int E, int N, mgg_dtype dtype,
                                         const mgg_routing* routing, int32_t* dev_status,
                                         void* stream) {
+  const mgg::NvtxRange nvtx("mgg_route_noalloc");
   using namespace mgg;
   if (!expert_ids || !topk_weights || !dev_status || !routing || !routing->counts ||
       !routing->end_offs || !routing->start || !routing->tile_start || !routing->row_assign ||
