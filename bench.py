@@ -495,6 +495,7 @@ def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush, peak_tf):
     res["dw_splitk"] = _dw_splitk_extra(dev, mgg, lib, flush)
     res["ffn_backward"] = _ffn_backward_extra(dev, mgg, lib, flush)
     res["fp8_backward_dx"] = _fp8_backward_dx_extra(dev, mgg, lib, flush, peaks, peak_kind)
+    res["step_tokens"] = _step_tokens_extra(dev, mgg, flush, peak_tf)
     fs, dec, be, bs = res["fwd_skew"], res["decode"], res["bare_e4"], res["bwd_split"]
     bwd_fl = 4.0 * 4096 * 2 * 2048 * 2048
     configs = {
@@ -512,6 +513,60 @@ def run_extras(dev, mgg, L, lib, peaks, peak_kind, flush, peak_tf):
         "5_decode": {"ms": dec["ms"], "GB/s": dec["GB/s"], "frac": dec["roofline"]["frac"]},
     }
     return res, configs
+
+
+def _step_tokens_extra(dev, mgg, flush, peak_tf):
+    """The same top-2 training step (K = N = 2048, E=8, k=2) at 2x and 4x the
+    headline's tokens, under the same CUDA-graph replay with the L2 flushed
+    before each step: how the step's fraction of the peak grows once the
+    fixed per-step costs (routing, backward prep, launch ramps) and the
+    partial last rounds weigh less."""
+    import torch
+    import workloads
+    out = {}
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for T in (8192, 16384):
+        p = workloads.moe_problem(T=T, K=2048, N=2048, E=8, k=2, seed=0, routing="uniform",
+                                  with_dy=True)
+        x, W, ids, w, dy = (p[n].to(dev) for n in ("x", "W", "expert_ids", "topk_weights", "dy"))
+        y = torch.empty(T, 2048, device=dev)
+        r = mgg.RoutingBuffers.empty(T, 2, 8, dev)
+        st = mgg.new_status(dev)
+        dx = torch.empty(T, 2048, device=dev)
+        dW = torch.empty(8, 2048, 2048, device=dev)
+        dt = torch.empty(T, 2, device=dev)
+
+        def step():
+            mgg.moe_forward(x, W, ids, w, out=y, routing=r, status=st)
+            mgg.moe_backward(dy, x, W, r, 2, status=st, dx=dx, dW=dW, dtopk=dt)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                step()
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        ts = []
+        for _ in range(20):
+            flush.zero_()
+            s0.record()
+            g.replay()
+            s1.record()
+            torch.cuda.synchronize()
+            ts.append(s0.elapsed_time(s1))
+        if mgg.read_status(st) != 0:
+            raise RuntimeError("step_tokens status set")
+        ms = statistics.mean(ts)
+        tf = 6.0 * T * 2 * 2048 * 2048 / (ms * 1e-3) / 1e12
+        out[f"T{T}"] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / peak_tf, 4)}
+        del x, W, ids, w, dy, y, r, dx, dW, dt, g
+        torch.cuda.empty_cache()
+    out["workload"] = ("fused MoE forward + backward, top-2, K=N=2048, E=8, k=2, uniform distinct "
+                       "routing, dy ~N(0,1), seed 0, at T = 8192 and 16384 tokens")
+    out["timing"] = "CUDA-graph replay of the step, 20 replays, L2 flushed before each"
+    return out
 
 
 def _fp8_backward_dx_extra(dev, mgg, lib, flush, peaks, peak_kind):
