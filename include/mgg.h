@@ -147,7 +147,8 @@ const char* mgg_status_string(mgg_status s);
  * Tile shape the library uses for an op (BM rows x BN columns, BK contraction
  * step), so callers can size schedules.  Returns MGG_ERR_DTYPE for an unknown
  * op/dtype pair.  For MGG_OP_FORWARD the routing's tile_start counts tiles of
- * this shape.
+ * this shape; for the gated-FFN ops (bf16 only) it counts the down GEMM's
+ * tiles, whose shape they return.
  */
 mgg_status mgg_tile_config(mgg_op op, mgg_dtype dtype, int* BM, int* BN, int* BK);
 

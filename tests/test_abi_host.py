@@ -104,6 +104,13 @@ def test_fp8_invalid_arguments_rejected_before_launch(lib):
     assert (bm.value, bn.value, bk.value) == (256, 256, 128)   # 128 codes per stage row
     assert lib.mgg_tile_config(L.MGG_OP_BACKWARD, L.MGG_FP8_E4M3, ctypes.byref(bm),
                                ctypes.byref(bn), ctypes.byref(bk)) == L.MGG_ERR_DTYPE
+    # the gated FFN: bf16 only, the down GEMM's pair tiles
+    for op in (L.MGG_OP_FFN_FORWARD, L.MGG_OP_FFN_BACKWARD):
+        assert lib.mgg_tile_config(op, L.MGG_BF16, ctypes.byref(bm), ctypes.byref(bn),
+                                   ctypes.byref(bk)) == 0
+        assert (bm.value, bn.value, bk.value) == (256, 256, 64)
+        assert lib.mgg_tile_config(op, L.MGG_F32, ctypes.byref(bm), ctypes.byref(bn),
+                                   ctypes.byref(bk)) == L.MGG_ERR_DTYPE
     # the e4m3 backward is the input gradient only: two schedule arrays of E+1
     assert lib.mgg_workspace_bytes(L.MGG_OP_BACKWARD, 64, 2, 8, 64, 64, L.MGG_FP8_E4M3) == 512
     # column quantiser: null, N not a multiple of 16, K not a multiple of 8,

@@ -412,6 +412,13 @@ mgg_status mgg_tile_config(mgg_op op, mgg_dtype dtype, int* BM, int* BN, int* BK
       *BN = bf ? kMaskedBI : kSimtBN;
       *BK = bf ? kBK : 16;
       return MGG_OK;
+    case MGG_OP_FFN_FORWARD:
+    case MGG_OP_FFN_BACKWARD:  // bf16 only; the routing's tiles are the down GEMM's
+      if (!bf) return MGG_ERR_DTYPE;
+      *BM = kPairBM;
+      *BN = kPairBN;
+      *BK = kBK;
+      return MGG_OK;
   }
   return MGG_ERR_DTYPE;
 }
