@@ -168,3 +168,16 @@ def test_noalloc_route_rejects_over_limit():
     s = lib.mgg_route_noalloc(ids.data_ptr(), w.data_ptr(), T, k, E, 64, L.MGG_BF16, ctypes.byref(rs),
                               st.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert s == L.MGG_ERR_WORKSPACE
+
+
+def test_python_wrapper_matches_route():
+    """mgg.route_noalloc (the torch wrapper) gives mgg.route's buffers."""
+    p = workloads.moe_problem(T=500, K=64, N=64, E=24, k=3, seed=41, routing="zipf")
+    ids, w = p["expert_ids"].to(DEV), p["topk_weights"].to(DEV)
+    st = mgg.new_status(DEV)
+    a = mgg.route_noalloc(ids, w, 24, 1536, status=st)
+    b = mgg.route(ids, w, 24, 1536, status=st)
+    torch.cuda.synchronize()
+    assert mgg.read_status(st) == 0
+    for f in FIELDS:
+        assert torch.equal(getattr(a, f), getattr(b, f)), f

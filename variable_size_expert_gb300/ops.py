@@ -23,7 +23,7 @@ import torch
 from . import _lib as L
 
 __all__ = [
-    "RoutingBuffers", "route", "moe_forward", "moe_backward", "moe", "grouped_gemm",
+    "RoutingBuffers", "route", "route_noalloc", "moe_forward", "moe_backward", "moe", "grouped_gemm",
     "grouped_gemm_masked", "debug_tile_schedule", "tile_config", "workspace_bytes",
     "moe_ffn_forward", "quantize_fp8", "moe_forward_fp8", "grouped_gemm_fp8",
     "grouped_gemm_masked_fp8", "quantize_fp8_cols", "moe_backward_dx_fp8",
@@ -136,6 +136,25 @@ def route(expert_ids: torch.Tensor, topk_weights: torch.Tensor, E: int, N: int,
     rs = r.struct()
     L.check(lib.mgg_route(_ptr(ids), _ptr(w), T, k, E, N, code, ctypes.byref(rs), _ptr(st),
                           _ptr(ws), ws.numel(), _stream()), "mgg_route")
+    return r
+
+
+def route_noalloc(expert_ids: torch.Tensor, topk_weights: torch.Tensor, E: int, N: int,
+                  dtype: torch.dtype = torch.bfloat16, status: torch.Tensor | None = None,
+                  out: RoutingBuffers | None = None) -> RoutingBuffers:
+    """``route`` without a workspace: the library's fixed device scratch
+    serves the histogram (mgg_route_noalloc; results as mgg_route)."""
+    lib = L.load()
+    ids = _ids_i32(expert_ids).contiguous()
+    w = topk_weights.contiguous().float()
+    T, k = ids.shape
+    dev = ids.device
+    r = out or RoutingBuffers.empty(T, k, E, dev)
+    st = status if status is not None else new_status(dev)
+    code = L.MGG_BF16 if dtype == torch.bfloat16 else L.MGG_F32
+    rs = r.struct()
+    L.check(lib.mgg_route_noalloc(_ptr(ids), _ptr(w), T, k, E, N, code, ctypes.byref(rs),
+                                  _ptr(st), _stream()), "mgg_route_noalloc")
     return r
 
 
