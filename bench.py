@@ -1018,7 +1018,7 @@ def _run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
         "roofline": {"bound": "tensor", "achieved": round(gemm_tf, 1), "peak": round(peak8, 1),
                      "unit": "TFLOP/s", "frac": round(gemm_tf / peak8, 4),
                      "peak_source": f"{peak_kind} bf16 dense (burst) x 2, the nominal e4m3/bf16 ratio",
-                     "traffic": None}}
+                     "traffic": load_traffic("fp8_fwd_gather_scatter_gemm")}}
     del xb, xq, sx, wq, sw, y8, r8
     # masked decode under CUDA-graph replay (inputs 3.8 GB >> L2)
     c = workloads.DECODE
@@ -1103,7 +1103,7 @@ def _run_extras(dev, mgg, L, lib, peaks, peak_kind, flush):
         "speedup_vs_bf16": round(ms / ms8, 3),
         "roofline": {"bound": "hbm", "achieved": round(gbs8, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(gbs8 / hbm, 4), "peak_source": f"{peak_kind} copy bandwidth",
-                     "traffic": None},
+                     "traffic": load_traffic("fp8_masked_decode_gemm")},
         "timing": "CUDA-graph replay, 20 replays"}
     del xq, sx, wq, sw, yd, g
     torch.cuda.empty_cache()
